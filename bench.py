@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on one B300 (or N independent replicas).
+
+Default workload: Qwen3-8B-shaped decode -- 1024 sequences, context = input U{100..1024} +
+generated U{100..1024}, 32 query / 8 KV heads, head_dim 128, block_size 256, 36 layer caches with
+random physical block placement. One step = for each of the 36 layers: kv_store of the newest
+token of every sequence, then paged decode attention over the whole context.
+
+Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle on a bounded sample of
+the same workload instead (the only reference implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV GB/s (% of HBM peak) and decode tokens/s at Qwen3-8B shapes"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, source):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel_key)
+    if not d or d.get("source_sha") != source_digest(source):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ------------------------------------------------------------------------------------------------
+# Workload set-up on the device
+# ------------------------------------------------------------------------------------------------
+
+
+class DecodeStep:
+    """All layers of one decode step, resident in HBM."""
+
+    def __init__(self, name, torch, pk, device, log_fill=True):
+        self.w = w = W.WORKLOADS[name]
+        self.torch, self.pk = torch, pk
+        self.ctx = W.decode_lengths(name)
+        self.B, self.L = len(self.ctx), w.num_layers
+        self.bt, self.nb = W.place_blocks(W.rng_for(w.seed, 10, 0), self.ctx, w.block_size)
+        self.slots = W.slots_for_positions(self.bt, np.arange(self.B), self.ctx - 1, w.block_size)
+        pool_shape = (self.nb, w.block_size, w.num_kv_heads, w.head_dim)
+        pool_bytes = 2 * int(np.prod(pool_shape)) * 2
+        free, _ = torch.cuda.mem_get_info(device)
+        per_layer_io = self.B * (2 * w.num_q_heads + 2 * w.num_kv_heads) * w.head_dim * 2
+        budget = free - 6 * (1 << 30) - self.L * per_layer_io
+        self.n_pools = int(max(1, min(self.L, budget // pool_bytes)))
+        t0 = time.time()
+        self.pools = []
+        for l in range(self.n_pools):
+            kc = torch.empty(pool_shape, dtype=torch.bfloat16, device=device)
+            vc = torch.empty(pool_shape, dtype=torch.bfloat16, device=device)
+            W.fill_normal_bf16_(kc, w.seed, 20 + l, 1)
+            W.fill_normal_bf16_(vc, w.seed, 20 + l, 2)
+            self.pools.append((kc, vc))
+        torch.cuda.synchronize()
+        if log_fill:
+            log(f"[bench] {self.n_pools} layer pools of {pool_bytes / 1e9:.2f} GB filled in "
+                f"{time.time() - t0:.1f} s")
+        mk = lambda shape, s: W.fill_normal_bf16_(  # noqa: E731
+            torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, 1000 + s)
+        self.q = [mk((self.B, w.num_q_heads, w.head_dim), 3 * l) for l in range(self.L)]
+        self.k_new = [mk((self.B, w.num_kv_heads, w.head_dim), 3 * l + 1) for l in range(self.L)]
+        self.v_new = [mk((self.B, w.num_kv_heads, w.head_dim), 3 * l + 2) for l in range(self.L)]
+        self.out = [torch.empty_like(x) for x in self.q]
+        self.bt_dev = torch.from_numpy(self.bt).to(device)
+        self.ctx_dev = torch.from_numpy(self.ctx).to(device)
+        self.slots_dev = torch.from_numpy(self.slots).to(device)
+        self.scale = 1.0 / np.sqrt(w.head_dim)
+        self.plan = pk.decode_plan(self.B, w.num_q_heads, self.pools[0][0], int(self.ctx.max()), 0)
+        self.ws = torch.empty(max(256, self.plan.workspace_bytes), dtype=torch.uint8,
+                              device=device)
+        self.kv_bytes_per_layer = int(self.ctx.sum()) * w.kv_bytes_per_token
+        self.launches_per_step = 3 * self.L  # store, decode plan, decode
+
+    def run(self, events=None):
+        pk = self.pk
+        for l in range(self.L):
+            kc, vc = self.pools[l % self.n_pools]
+            pk.kv_store(self.k_new[l], self.v_new[l], self.slots_dev, kc, vc)
+            if events is not None:
+                events[l][0].record()
+            pk.paged_decode(self.q[l], kc, vc, self.bt_dev, self.ctx_dev, self.scale,
+                            out=self.out[l], plan=self.plan, workspace=self.ws)
+            if events is not None:
+                events[l][1].record()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle arm
+# ------------------------------------------------------------------------------------------------
+
+
+def oracle_sample_case(name, n_seqs):
+    """A host-side sample of the workload: n_seqs sequences of one layer, drawn on the host."""
+    w = W.WORKLOADS[name]
+    ctx = W.decode_lengths(name)[:n_seqs]
+    return W.random_decode_case(w.seed, n_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                w.block_size, 0, 0, context_lens=ctx)
+
+
+def time_oracle(name, target_s=12.0, max_seqs=256):
+    """Time the oracle (store + decode of one layer) on a sample sized to about target_s."""
+    import oracle
+    orc = oracle.default()
+    w = W.WORKLOADS[name]
+    n = 8
+    while True:
+        case = oracle_sample_case(name, n)
+        t0 = time.perf_counter()
+        kc, vc, _ = orc.kv_store(case.k_new, case.v_new, case.slot_mapping, case.k_cache,
+                                 case.v_cache)
+        orc.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or n >= max_seqs:
+            break
+        n = min(max_seqs, max(n + 1, int(n * target_s / 4 / max(dt, 1e-3))))
+    kv = int(case.context_lens.sum()) * w.kv_bytes_per_token
+    return dict(n_seqs=n, seconds=dt, kv_bytes=kv, cores=orc.max_threads(),
+                gbs=kv / dt / 1e9, tokens_per_s=n / (dt * w.num_layers))
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    orc = oracle.default()
+    w = W.WORKLOADS[args.workload]
+    probe = time_oracle(args.workload, target_s=4.0, max_seqs=64)
+    n = probe["n_seqs"]
+    case = oracle_sample_case(args.workload, n)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        kc, vc, _ = orc.kv_store(case.k_new, case.v_new, case.slot_mapping, case.k_cache,
+                                 case.v_cache)
+        orc.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    kv = int(case.context_lens.sum()) * w.kv_bytes_per_token
+    dt = sum(times) / len(times)
+    value = kv / dt / 1e9
+    sample = (f"{n} of {w.num_seqs} sequences of one of {w.num_layers} layers per step "
+              f"(store of the newest token + decode, fp64)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "decode_tokens_per_s": n / (dt * w.num_layers),
+        "config": {"workload": args.workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_decode")
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import paged_kv_cache_496_b300 as pk
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_uuid = str(getattr(props, "uuid", "") or "")
+    if gpu_uuid and not gpu_uuid.startswith("GPU-"):
+        gpu_uuid = "GPU-" + gpu_uuid
+
+    step = DecodeStep(args.workload, torch, pk, device)
+    w = step.w
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- warm-up, then the timed region ----
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert pk.get_device_error() == 0, "device error flag raised during warm-up"
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(step.L)]
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_uuid) as clocks:
+        start.record()
+        for i in range(args.steps):
+            step.run(evs[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(stop) / args.steps)
+    decode_ms = [e[0].elapsed_time(e[1]) for s in evs for e in s]
+    decode_ms_mean = max_over_ranks(sum(decode_ms) / len(decode_ms))
+    flags = pk.get_device_error()
+    if flags:
+        log(f"[bench] device error flags {flags:#x}")
+
+    kv_step = step.kv_bytes_per_layer * step.L
+    value = kv_step * world / (ms / 1e3) / 1e9
+    tokens_per_s = step.B * world / (ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    achieved = step.kv_bytes_per_layer / (decode_ms_mean / 1e3) / 1e9
+    traffic = profiled_traffic("paged_decode_qwen3_8b",
+                               os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc",
+                                            "paged_decode.cu"))
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if True:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_q = [pin(x) for x in step.q]
+        h_k = [pin(x) for x in step.k_new]
+        h_v = [pin(x) for x in step.v_new]
+        h_bt, h_ctx, h_sl = pin(step.bt_dev), pin(step.ctx_dev), pin(step.slots_dev)
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in step.out]
+        h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_bt, h_ctx, h_sl])
+        d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+        def e2e_step():
+            step.bt_dev.copy_(h_bt, non_blocking=True)
+            step.ctx_dev.copy_(h_ctx, non_blocking=True)
+            step.slots_dev.copy_(h_sl, non_blocking=True)
+            for l in range(step.L):
+                step.q[l].copy_(h_q[l], non_blocking=True)
+                step.k_new[l].copy_(h_k[l], non_blocking=True)
+                step.v_new[l].copy_(h_v[l], non_blocking=True)
+                kc, vc = step.pools[l % step.n_pools]
+                pk.kv_store(step.k_new[l], step.v_new[l], step.slots_dev, kc, vc)
+                pk.paged_decode(step.q[l], kc, vc, step.bt_dev, step.ctx_dev, step.scale,
+                                out=step.out[l], plan=step.plan, workspace=step.ws)
+                h_out[l].copy_(step.out[l], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        e2e = {"value": kv_step * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+               "ms_per_step": e2e_ms, "decode_tokens_per_s": step.B * world / (e2e_ms / 1e3),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    extras = {}
+    if not args.no_extras:
+        extras = secondary_measurements(torch, pk, device, step)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle(args.workload)
+        cpu = {"value": r["gbs"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+               "sample": f"{r['n_seqs']} sequences x 1 layer (store + decode), "
+                         f"{r['seconds']:.1f} s, KV GB/s of the sample",
+               "decode_tokens_per_s": r["tokens_per_s"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "accumulate": "fp32", "data": "synthetic",
+            "decode_tokens_per_s": tokens_per_s, "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "config": {"workload": args.workload, "num_seqs": step.B, "num_layers": step.L,
+                       "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "block_size": w.block_size,
+                       "context": "input U{100..1024} + generated U{100..1024}",
+                       "mean_context": float(step.ctx.mean()),
+                       "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
+                       "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
+                       "step": "per layer: kv_store (1 token/seq) + paged_decode",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "paged_decode (plan + persistent decode kernel)",
+                         "algorithmic_bytes_per_launch": step.kv_bytes_per_layer,
+                         "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind},
+            "clocks": clocks.summary(),
+            "gpu_launches": step.launches_per_step * args.steps,
+            "device_error_flags": flags,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "components": extras,
+            "gpu": props.name,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def secondary_measurements(torch, pk, device, main_step):
+    """Other rows of the hot path, each timed on its own (not part of the step above)."""
+    res = {}
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    # kv_store alone at the decode size (launch-bound) and at the prefill size (bandwidth-bound)
+    kc, vc = main_step.pools[0]
+    ms = timed(lambda: pk.kv_store(main_step.k_new[0], main_step.v_new[0], main_step.slots_dev,
+                                   kc, vc))
+    row = main_step.w.kv_bytes_per_token // 2
+    res["kv_store_1024_tokens"] = {"ms": ms, "GB/s": 2 * 2 * main_step.B * row / ms / 1e6}
+    T = 35968
+    rng = W.rng_for(4, 300)
+    slots = torch.from_numpy(rng.permutation(main_step.nb * 256)[:T].astype(np.int32)).to(device)
+    kn = W.fill_normal_bf16_(torch.empty((T, 8, 128), dtype=torch.bfloat16, device=device),
+                             4, 301)
+    ms = timed(lambda: pk.kv_store(kn, kn, slots, kc, vc))
+    res["kv_store_35968_tokens"] = {"ms": ms, "GB/s": 2 * 2 * T * row / ms / 1e6}
+
+    # long-context split decode (one layer)
+    try:
+        layer = _decode_layer("long_splitk_decode", torch, device)
+        ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
+                                           layer["ctx"], layer["scale"], out=layer["out"],
+                                           plan=layer["plan"], workspace=layer["ws"]))
+        res["long_splitk_decode"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6}
+        del layer
+    except Exception as e:  # report, do not hide
+        res["long_splitk_decode"] = {"error": repr(e)}
+    try:
+        layer = _decode_layer("qwen3_0p6b_decode", torch, device)
+        ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
+                                           layer["ctx"], layer["scale"], out=layer["out"],
+                                           plan=layer["plan"], workspace=layer["ws"]))
+        res["qwen3_0p6b_decode_layer"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6}
+        del layer
+    except Exception as e:
+        res["qwen3_0p6b_decode_layer"] = {"error": repr(e)}
+    return res
+
+
+def _decode_layer(name, torch, device):
+    import paged_kv_cache_496_b300 as pk
+    w = W.WORKLOADS[name]
+    ctx = W.decode_lengths(name)
+    bt, nb = W.place_blocks(W.rng_for(w.seed, 10, 0), ctx, w.block_size)
+    shape = (nb, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = W.fill_normal_bf16_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, 1)
+    vc = W.fill_normal_bf16_(torch.empty(shape, dtype=torch.bfloat16, device=device), w.seed, 2)
+    q = W.fill_normal_bf16_(torch.empty((len(ctx), w.num_q_heads, w.head_dim),
+                                        dtype=torch.bfloat16, device=device), w.seed, 3)
+    plan = pk.decode_plan(len(ctx), w.num_q_heads, kc, int(ctx.max()), 0)
+    return dict(q=q, kc=kc, vc=vc, bt=torch.from_numpy(bt).to(device),
+                ctx=torch.from_numpy(ctx).to(device), scale=1.0 / np.sqrt(w.head_dim),
+                out=torch.empty_like(q), plan=plan,
+                ws=torch.empty(max(256, plan.workspace_bytes), dtype=torch.uint8, device=device),
+                kv=int(ctx.sum()) * w.kv_bytes_per_token)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,180 @@
+/*
+ * pagedkv.h -- C ABI of the B300 (sm_103a) paged KV-cache hot path: KV store, paged decode
+ * attention, varlen paged prefill attention.
+ *
+ * The operations follow the PagedAttention scheme described on the source pages:
+ *  [P1] "DeepSeek研究员1200行代码复刻vLLM，H800硬件实测性能反超原版" (QbitAI), section "vLLM是什么？":
+ *       the KV cache is divided into fixed-size blocks; a per-sequence block table maps logical
+ *       blocks to physical blocks; keys and values of one sequence live in blocks that need not be
+ *       contiguous; the attention kernel fetches the blocks one by one; KV may be shared within
+ *       and across requests.
+ *  [P3] "nano-vllm 深度分析报告": table "可复用的模式与技巧", row "slot_mapping -1 padding"
+ *       (slots padded for CUDA graphs are -1 and the store skips them); table "关键设计决策"
+ *       (block_size 256 versus vLLM's 16); section "创新之处" (prefix-cache hits share physical
+ *       blocks; CUDA graphs captured for a ladder of batch sizes).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller; the library never
+ *    allocates, frees or retains them. bf16 tensors are passed as `uint16_t*` holding bf16 bit
+ *    patterns. All device pointers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as `void*` (NULL = the legacy default stream). Work is only
+ *    enqueued; no call synchronises the device, so the calls can be captured into a CUDA graph.
+ *  - Cache layout: k_cache and v_cache are [num_blocks, block_size, num_kv_heads, head_dim] bf16,
+ *    row-major. The token at slot s lives at block s / block_size, offset s % block_size.
+ *  - Grouped-query attention: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Return value: PKV_OK (0) or a negative PKV_ERR_* code. On error nothing is enqueued and a
+ *    message is available from pkv_last_error() (thread-local). No exception crosses the ABI.
+ *  - Bad data inside device buffers (a slot or block id out of range, a context longer than its
+ *    block table) cannot be checked on the host without a synchronisation. The kernels check it,
+ *    skip the offending access (they never read or write out of range) and set a bit in a device
+ *    error word that pkv_get_device_error() reads back.
+ *  - Supported shapes: head_dim 64 or 128; block_size a power of two from 16 to 256;
+ *    num_q_heads a multiple of num_kv_heads with group size 1, 2, 4 or 8;
+ *    num_blocks * block_size < 2^31.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)        /* null pointer, bad size, misaligned pointer */
+#define PKV_ERR_UNSUPPORTED (-2)        /* valid but unsupported shape (see above) */
+#define PKV_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below what the plan needs */
+#define PKV_ERR_CUDA (-4)               /* a CUDA runtime / driver call failed */
+
+/* Bits of the device error word (pkv_get_device_error). */
+#define PKV_DEVERR_BAD_SLOT 1       /* kv_store: slot neither -1 nor in [0, num_blocks*block_size) */
+#define PKV_DEVERR_BAD_BLOCK 2      /* a block table entry outside [0, num_blocks) was needed */
+#define PKV_DEVERR_CTX_CLAMPED 4    /* a context longer than its block table or the decode plan */
+#define PKV_DEVERR_TIMEOUT 8        /* an internal pipeline wait gave up after one second */
+#define PKV_DEVERR_BAD_LENGTHS 16   /* prefill: cu_seqlens not increasing or k_len < q_len */
+
+/* Geometry of one layer's paged cache. */
+typedef struct pkv_cache_desc {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+} pkv_cache_desc;
+
+/*
+ * KV store [P3 "slot_mapping -1 padding"; P1 fixed-size blocks].
+ * For t in [0, num_tokens): s = slot_mapping[t]; if s == -1 the token is skipped; otherwise
+ * k[t] is copied bit for bit to k_cache[s / block_size][s % block_size] and v[t] likewise.
+ *   k, v          device, [num_tokens, num_kv_heads, head_dim] bf16
+ *   slot_mapping  device, [num_tokens] int32
+ *   k_cache, v_cache  device, cache layout above (written in place)
+ * Duplicate slots in one call are a caller error (which row wins is unspecified).
+ * num_tokens == 0 is a no-op.
+ */
+PKV_API int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping,
+                 int32_t num_tokens, uint16_t* k_cache, uint16_t* v_cache, pkv_cache_desc cache,
+                 void* stream);
+
+/*
+ * Decode plan: how pkv_paged_decode cuts contexts into chunks (flash-decoding split) and how much
+ * device workspace it needs. A pure host computation (no CUDA call).
+ *   max_context_len    an upper bound of every context length the plan will be used with
+ *   split_tokens_hint  0 = automatic: contexts longer than 512 tokens may be split, and the
+ *                      device picks the chunk length (>= 512) from the actual lengths so that
+ *                      the work spreads over all SMs; a large batch is then not split at all.
+ *                      > 0 = fixed chunk length (rounded up to a multiple of 128).
+ *                      < 0 = never split.
+ * Outputs: split_tokens (fixed chunk length, or the smallest chunk length when auto_split is 1),
+ * max_splits (the most chunks any sequence can have), workspace_bytes (device workspace the
+ * decode call needs for these num_seqs and num_q_heads).
+ */
+typedef struct pkv_decode_plan {
+  int32_t split_tokens;
+  int32_t max_splits;
+  int32_t auto_split;
+  int32_t max_context_len;
+  size_t workspace_bytes;
+} pkv_decode_plan;
+
+PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
+                         int32_t max_context_len, int32_t split_tokens_hint,
+                         pkv_decode_plan* plan);
+
+/*
+ * Paged decode attention [P1 PagedAttention].
+ * For sequence b and query head h (kv head g = h / G):
+ *   out[b][h] = softmax(scale * q[b][h] . K_b^T) V_b
+ * over the context_lens[b] tokens at positions 0 .. context_lens[b]-1, where position p of
+ * sequence b lives at block block_tables[b][p / block_size], offset p % block_size. A sequence
+ * with context_lens[b] == 0 (a padded batch entry) gets zeros. Chunks of a split context are
+ * merged with their log-sum-exp weights inside the same launch sequence.
+ *   q             device, [num_seqs, num_q_heads, head_dim] bf16
+ *   block_tables  device, [num_seqs, max_blocks_per_seq] int32 (entries past the context unused)
+ *   context_lens  device, [num_seqs] int32, each <= plan->max_context_len and
+ *                 <= max_blocks_per_seq * block_size (longer contexts are clamped and flagged)
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim))
+ *   plan          host, from pkv_decode_plan_make with the same num_seqs, num_q_heads, cache
+ *   out           device, [num_seqs, num_q_heads, head_dim] bf16 (fp32 accumulation, RNE)
+ *   workspace     device scratch of at least plan->workspace_bytes, 256-byte aligned, owned by
+ *                 the caller. Every call rewrites it, so calls that share one workspace must be
+ *                 ordered on one stream.
+ * Launches: a one-CTA plan kernel (chunking, work list) and the persistent decode kernel.
+ */
+PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     pkv_cache_desc cache, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                     int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+                     uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Varlen causal paged prefill [P1 PagedAttention; P3 prefix-cache hits share blocks].
+ * Sequence b has q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens (rows cu_seqlens_q[b] ..
+ * of q, k, v) and k_len = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys. The first P = k_len - q_len
+ * keys are a cached prefix (possibly blocks shared with other sequences); the rest are the new
+ * tokens. New query i attends keys 0 .. P + i (causal, aligned to the end).
+ *   q             device, [total_q, num_q_heads, head_dim] bf16
+ *   k, v          device, [total_q, num_kv_heads, head_dim] bf16: the new tokens
+ *   cu_seqlens_q, cu_seqlens_k  device, [num_seqs + 1] int32, non-decreasing, starting at 0
+ *   max_seqlen_q  host int, >= every q_len
+ *   block_tables  device [num_seqs, max_blocks_per_seq] int32, or NULL.
+ *       Non-NULL: every key (prefix and new) is read through the block table, so the new tokens
+ *       must already have been stored with pkv_kv_store (as the engine does before attention).
+ *       NULL: there is no prefix (cu_seqlens_k must equal cu_seqlens_q) and keys are read from
+ *       k and v directly; k_cache and v_cache may then be NULL.
+ *   out           device, [total_q, num_q_heads, head_dim] bf16
+ */
+PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+                      int32_t total_q, int32_t max_seqlen_q, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const uint16_t* k_cache,
+                      const uint16_t* v_cache, pkv_cache_desc cache, int32_t num_q_heads,
+                      float scale, uint16_t* out, void* stream);
+
+/*
+ * Read and clear the device error word of the current device (PKV_DEVERR_* bits). Synchronises
+ * the device first; not for use inside stream capture.
+ */
+PKV_API int pkv_get_device_error(int32_t* flags);
+
+/* Text for a PKV_* status code (static storage). */
+PKV_API const char* pkv_status_string(int status);
+
+/* Message for the last failing call on this thread ("" if none). */
+PKV_API const char* pkv_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+PKV_API int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,315 @@
+// abi.cu -- the extern "C" entry points of libpagedkv.so (declared in include/pagedkv.h).
+//
+// Host-side argument validation, TMA descriptor encoding, the per-device error word and status
+// strings. Every entry point only enqueues work on the caller's stream; nothing here allocates
+// device memory.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Device error word: one per device (each device has its own copy of a __device__ variable).
+__device__ int g_device_flags = 0;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int* flags = nullptr;
+  int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_flags);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.flags = static_cast<int*>(p);
+    d.num_sms = sms;
+    d.ready = true;
+  }
+  *out = d;
+  return PKV_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no link to libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn* fn) {
+  static std::once_flag once;
+  static EncodeTiledFn encoder = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                           &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      encoder = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  if (encoder == nullptr)
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(err));
+  *fn = encoder;
+  return PKV_OK;
+}
+
+// 3-D view {D, heads, rows} of a row-major [rows, heads, D] bf16 tensor; box {box_d, 1, box_rows}.
+int encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int head_dim,
+                    int box_d, int box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc;
+  int st = get_encoder(&enc);
+  if (st != PKV_OK) return st;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int check_cache(const pkv_cache_desc& c) {
+  if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "cache geometry must be positive");
+  if (c.head_dim != 64 && c.head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c.head_dim);
+  if (!is_pow2(c.block_size) || c.block_size < 16 || c.block_size > 256)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: powers of two 16..256)",
+                c.block_size);
+  if ((int64_t)c.num_blocks * c.block_size >= ((int64_t)1 << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "num_blocks * block_size must be below 2^31");
+  return PKV_OK;
+}
+
+int check_heads(int num_q_heads, int num_kv_heads) {
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                num_q_heads, num_kv_heads);
+  const int G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(PKV_ERR_UNSUPPORTED, "group size %d (supported: 1, 2, 4, 8)", G);
+  return PKV_OK;
+}
+
+constexpr int32_t kAutoSplitFloor = 512;
+
+int32_t round_up(int64_t x, int64_t q) { return (int32_t)((x + q - 1) / q * q); }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int pkv_get_device_error(int32_t* flags) {
+  if (flags == nullptr) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
+  DeviceInfo d;
+  int st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, d.flags, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  const int zero = 0;
+  e = cudaMemcpy(d.flags, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  *flags = v;
+  return PKV_OK;
+}
+
+int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping,
+                 int32_t num_tokens, uint16_t* k_cache, uint16_t* v_cache, pkv_cache_desc cache,
+                 void* stream) {
+  g_last_error[0] = 0;
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
+  DeviceInfo d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_kv_store(k, v, slot_mapping, num_tokens, k_cache, v_cache, cache,
+                                  d.num_sms, d.flags, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_store launch");
+  return PKV_OK;
+}
+
+int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
+                         int32_t max_context_len, int32_t split_tokens_hint,
+                         pkv_decode_plan* plan) {
+  g_last_error[0] = 0;
+  if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  st = check_heads(num_q_heads, cache.num_kv_heads);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_context_len < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs and max_context_len must be >= 0");
+  const int64_t ctx = max_context_len > 0 ? max_context_len : 1;
+  pkv_decode_plan pl;
+  memset(&pl, 0, sizeof pl);
+  pl.max_context_len = max_context_len;
+  if (split_tokens_hint < 0 || (split_tokens_hint == 0 && ctx <= kAutoSplitFloor)) {
+    pl.split_tokens = round_up(ctx, kSplitQuantum);
+    pl.max_splits = 1;
+    pl.auto_split = 0;
+  } else if (split_tokens_hint > 0) {
+    pl.split_tokens = round_up(split_tokens_hint, kSplitQuantum);
+    pl.max_splits = (int32_t)((ctx + pl.split_tokens - 1) / pl.split_tokens);
+    pl.auto_split = 0;
+  } else {
+    pl.split_tokens = kAutoSplitFloor;
+    pl.max_splits = (int32_t)((ctx + kAutoSplitFloor - 1) / kAutoSplitFloor);
+    pl.auto_split = 1;
+  }
+  pl.workspace_bytes =
+      decode_workspace_bytes(num_seqs, num_q_heads, cache.head_dim, pl.max_splits, nullptr,
+                             nullptr);
+  *plan = pl;
+  return PKV_OK;
+}
+
+int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     pkv_cache_desc cache, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                     int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+                     uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error[0] = 0;
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  st = check_heads(num_q_heads, cache.num_kv_heads);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d < 0", num_seqs);
+  if (num_seqs == 0) return PKV_OK;
+  if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->split_tokens <= 0 || plan->split_tokens % kSplitQuantum != 0 ||
+      plan->max_splits <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "malformed decode plan");
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(PKV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+    return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  DecodeArgs a;
+  const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
+                                             plan->max_splits, &a.ws, workspace);
+  if (workspace_bytes < need)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, plan needs %zu",
+                workspace_bytes, need);
+  DeviceInfo d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  const int G = num_q_heads / cache.num_kv_heads;
+  const int GH = G >= 4 ? 4 : G;
+  const int tile = 128 / GH;
+  const int box_t = cache.block_size < tile ? cache.block_size : tile;
+  CUtensorMap tk, tv;
+  const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
+  st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
+                       box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != PKV_OK) return st;
+  st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
+                       box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != PKV_OK) return st;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cache = cache;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.split_tokens = plan->split_tokens;
+  a.max_splits = plan->max_splits;
+  a.auto_split = plan->auto_split != 0;
+  a.out = out;
+  a.flags = d.flags;
+  cudaError_t e = launch_paged_decode(a, tk, tv, d.num_sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return fail(PKV_ERR_UNSUPPORTED, "no decode instance");
+  if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
+  return PKV_OK;
+}
+
+int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+                      int32_t total_q, int32_t max_seqlen_q, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const uint16_t* k_cache,
+                      const uint16_t* v_cache, pkv_cache_desc cache, int32_t num_q_heads,
+                      float scale, uint16_t* out, void* stream) {
+  g_last_error[0] = 0;
+  (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)num_seqs;
+  (void)total_q; (void)max_seqlen_q; (void)block_tables; (void)max_blocks_per_seq;
+  (void)k_cache; (void)v_cache; (void)cache; (void)num_q_heads; (void)scale; (void)out;
+  (void)stream;
+  return fail(PKV_ERR_UNSUPPORTED, "paged_prefill is not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// kernels.h -- launchers of the paged KV-cache kernels (internal to libpagedkv.so).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// Tokens per decode tile for a given number of query heads per CTA; split chunks are multiples
+// of the largest tile (128 tokens).
+constexpr int kSplitQuantum = 128;
+
+struct DecodeWorkspace {
+  uint32_t* header;    // [0] claim counter, [1] number of items, [2] chunk length (tokens)
+  int2* items;         // (sequence, chunk) pairs, B * max_splits entries at most
+  uint32_t* counters;  // chunks finished per (sequence, head group, consumer warp)
+  float* part_acc;     // [B, max_splits, Hq, D] un-normalised partial outputs
+  float2* part_ml;     // [B, max_splits, Hq, D / 64] (running max in log2 units, denominator)
+};
+
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                              int32_t max_splits, DecodeWorkspace* carve, void* base);
+
+cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping,
+                            int32_t num_tokens, uint16_t* k_cache, uint16_t* v_cache,
+                            const pkv_cache_desc& cache, int num_sms, int* flags,
+                            cudaStream_t stream);
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  pkv_cache_desc cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  float scale;
+  int32_t split_tokens;  // chunk length (fixed) or smallest chunk length (auto), multiple of 128
+  int32_t max_splits;    // ceil(max_context_len / split_tokens)
+  bool auto_split;       // choose the chunk length on the device from the actual lengths
+  uint16_t* out;
+  DecodeWorkspace ws;
+  int* flags;
+};
+
+// Returns a CUDA error, or cudaErrorNotSupported for shapes without an instance.
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tmap_k,
+                                const CUtensorMap& tmap_v, int num_sms, cudaStream_t stream);
+
+struct PrefillArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_seqlen_q;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  pkv_cache_desc cache;
+  int32_t num_q_heads;
+  float scale;
+  uint16_t* out;
+  int* flags;
+};
+
+cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tmap_q,
+                                 const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                 int num_sms, cudaStream_t stream);
+
+}  // namespace pkv

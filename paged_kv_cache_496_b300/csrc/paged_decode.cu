@@ -1,0 +1,796 @@
+// paged_decode.cu -- paged decode attention (one query per sequence) for sm_103a.
+//
+// Source: "DeepSeek研究员1200行代码复刻vLLM，H800硬件实测性能反超原版" (QbitAI), section
+// "vLLM是什么？": keys and values of a sequence sit in fixed-size blocks found through its block
+// table, and the attention kernel fetches the blocks one by one. The result is ordinary softmax
+// attention over the sequence's tokens; only the addressing is paged.
+//
+// Design (B300-first, not a translation of any earlier kernel):
+//  * Work item = (sequence b, group of GH query heads sharing one kv head, context chunk s).
+//    A one-CTA plan kernel turns context_lens into a list of (b, s) items on the device, so the
+//    host never synchronises; a persistent grid claims items with an atomic counter and keeps
+//    its TMA pipeline full across item boundaries.
+//  * Warp specialisation: one producer warp walks the block table (32 entries per coalesced
+//    load, kept in registers) and issues one 3-D TMA box per (block, tile) for K and for V into a
+//    multi-stage shared-memory ring guarded by mbarriers; four consumer warps compute.
+//  * Consumers: eight lanes share one token row (each lane owns D/8 of the dims), 8/GH tokens per
+//    lane group, so the q.k partial sums of 8 (token, head) pairs are reduced with a 7-shuffle
+//    reduce-scatter that leaves exactly one score per lane. Online softmax runs in log2 units in
+//    fp32 with a lazy rescale (only when a head's max grows by more than 2^8); products use the
+//    packed fp32x2 FMA. The four warps' partial (max, sum, acc) are merged through shared memory.
+//  * Long contexts are cut into chunks (flash-decoding split). The plan kernel picks the chunk
+//    length from the actual total work (so a few long sequences are spread over all SMs while a
+//    large batch is not split at all). A chunk writes fp32 partials (un-normalised acc, running
+//    max, denominator) to the caller's workspace; the CTA that finishes the last chunk of a
+//    (sequence, head group) merges them with log-sum-exp weights, so no extra launch is needed.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kMetaFirst = 1;  // first tile of an item: load q, reset the running state
+constexpr int kMetaLast = 2;   // last tile of an item: merge warps and write the result
+constexpr int kMetaZero = 4;   // an item with no tokens (context 0): write zeros
+constexpr int kMetaDone = 8;   // no more items
+constexpr float kTau = 8.0f;   // lazy-rescale threshold (log2 units)
+
+struct alignas(16) StageMeta {
+  int32_t b, x, split, nsplit;
+  int32_t tok0, tok_end, flags, pad;
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  uint16_t* out;
+  float* part_acc;
+  float2* part_ml;
+  const int2* items;
+  uint32_t* header;    // [0] claim counter, [1] item count, [2] chunk length in tokens
+  uint32_t* counters;  // per (sequence, head group, consumer warp): chunks finished
+  int* flags;
+  int32_t max_blocks;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t head_groups;     // groups of GH query heads: num_q_heads / GH
+  int32_t groups_per_kv;   // head groups that share one kv head: (Hq / Hkv) / GH
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_splits;
+  int32_t cap_tokens;  // contexts are clamped to this many tokens (table and plan capacity)
+  float qk_scale_log2;
+};
+
+template <int D, int GH>
+struct Traits {
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = (kWarps + 1) * 32;
+  static constexpr int kTPG = 8 / GH;                  // tokens per lane group per tile
+  static constexpr int kTokPerWarp = 4 * kTPG;
+  static constexpr int kTileT = kWarps * kTokPerWarp;  // 128 / GH tokens per tile
+  static constexpr int kChunks = D / 64;               // 16-byte chunks per lane per row
+  static constexpr int kPairs = D / 16;                // fp32 pairs per lane per row
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kTileBytes = kTileT * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQBytes = GH * D * 2;
+  // acc [GH][D], then m [GH], then l [GH]; padded so every warp's slot is 16-byte aligned
+  static constexpr int kCbFloats = (GH * D + 2 * GH + 3) / 4 * 4;
+  // Two CTAs per SM: keep each CTA within 112 KB of shared memory.
+  static constexpr int kSmemBudget = 112 * 1024;
+  static constexpr int kFixedBytes = 2 * kWarps * kCbFloats * 4 + 8 * 32 + 160;
+  static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / (kStageBytes + kQBytes);
+  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+  static constexpr int kMaxSub = kTileT / 16;        // TMA boxes per tile at block_size 16
+  static constexpr int kOffTiles = 0;
+  static constexpr int kOffQ = kOffTiles + kStages * kStageBytes;
+  static constexpr int kOffCb = kOffQ + kStages * kQBytes;
+  static constexpr int kOffMeta = kOffCb + 2 * kWarps * kCbFloats * 4;
+  static constexpr int kOffBar = (kOffMeta + kStages * (int)sizeof(StageMeta) + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
+  static_assert(kTPG * GH == 8, "one (token, head) score per lane of a group");
+  static_assert(kCbFloats % 4 == 0, "float4 stores into the combine slots");
+  static_assert(kQBytes % 16 == 0 && kOffQ % 128 == 0 && kOffCb % 16 == 0, "smem alignment");
+  static_assert(kOffMeta % 16 == 0 && kOffBar % 16 == 0, "smem alignment");
+  static_assert(kStageBytes % 1024 == 0 && kTileBytes % 1024 == 0, "TMA destinations");
+};
+
+// ---------------------------------------------------------------------------------------------
+// Plan: context_lens -> chunk length and list of (sequence, chunk) items; resets the counters.
+// ---------------------------------------------------------------------------------------------
+
+constexpr int kPlanThreads = 1024;
+constexpr int kChunksPerSlot = 8;  // aim for this many chunks per resident CTA when splitting
+
+struct PlanParams {
+  const int32_t* context_lens;
+  int2* items;
+  uint32_t* header;
+  uint32_t* counters;
+  int* flags;
+  int32_t num_seqs;
+  int32_t cap_tokens;
+  int32_t split_floor;   // smallest chunk length (tokens, multiple of 128)
+  int32_t fixed_split;   // > 0: use exactly this chunk length
+  int32_t head_groups;
+  int32_t slots;         // resident CTAs of the decode grid
+  int32_t num_counters;  // entries of `counters` to zero (0 when nothing is split)
+};
+
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t r = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0u);
+  *total = warp_sums[31];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanParams pp) {
+  __shared__ uint32_t warp_sums[32];
+  __shared__ int32_t split_sh;
+  const int tid = threadIdx.x;
+  const int per = (pp.num_seqs + kPlanThreads - 1) / kPlanThreads;
+  const int b0 = min(pp.num_seqs, tid * per);
+  const int b1 = min(pp.num_seqs, b0 + per);
+  for (int i = tid; i < pp.num_counters; i += kPlanThreads) pp.counters[i] = 0u;
+  // total tokens (for the chunk length) -- in units of 16 tokens to stay within 32 bits
+  uint32_t local_tok = 0;
+  for (int b = b0; b < b1; ++b) {
+    int ctx = pp.context_lens[b];
+    if (ctx > pp.cap_tokens) {
+      raise_flag(pp.flags, PKV_DEVERR_CTX_CLAMPED);
+      ctx = pp.cap_tokens;
+    }
+    local_tok += ctx > 0 ? (uint32_t)((ctx + 15) / 16) : 0u;
+  }
+  uint32_t total16 = 0;
+  block_exclusive_scan(local_tok, warp_sums, &total16);
+  if (tid == 0) {
+    int32_t S = pp.fixed_split;
+    if (S <= 0) {
+      // chunk so that every resident CTA sees about kChunksPerSlot chunks of work
+      const double per_slot = (double)total16 * 16.0 * pp.head_groups / (double)pp.slots;
+      double want = per_slot / kChunksPerSlot;
+      if (want > (double)pp.cap_tokens) want = (double)pp.cap_tokens;
+      int64_t w = ((int64_t)want + 127) / 128 * 128;
+      if (w < pp.split_floor) w = pp.split_floor;
+      S = (int32_t)w;
+    }
+    split_sh = S;
+    pp.header[2] = (uint32_t)S;
+  }
+  __syncthreads();
+  const int32_t S = split_sh;
+  uint32_t local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int ctx = min(pp.context_lens[b], pp.cap_tokens);
+    local += ctx > 0 ? (uint32_t)((ctx + S - 1) / S) : 1u;
+  }
+  uint32_t total = 0;
+  uint32_t pos = block_exclusive_scan(local, warp_sums, &total);
+  for (int b = b0; b < b1; ++b) {
+    const int ctx = min(pp.context_lens[b], pp.cap_tokens);
+    const int n = ctx > 0 ? (ctx + S - 1) / S : 1;
+    for (int s = 0; s < n; ++s) pp.items[pos++] = make_int2(b, s);
+  }
+  if (tid == 0) {
+    pp.header[1] = total;  // number of (sequence, chunk) items
+    pp.header[0] = 0u;     // claim counter
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Register-level pieces of the consumer
+// ---------------------------------------------------------------------------------------------
+
+// Eight partial sums per lane, one per (token, head) pair of the lane group, summed over the
+// group's eight lanes; afterwards lane j of the group holds the full sum of pair j.
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int j) {
+  {
+    const bool up = j & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = up ? v[i] : v[i + 4];
+      const float keep = up ? v[i + 4] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, 4);
+    }
+  }
+  {
+    const bool up = j & 2;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up ? v[i] : v[i + 2];
+      const float keep = up ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, 2);
+    }
+  }
+  {
+    const bool up = j & 1;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(kFullMask, send, 1);
+  }
+  return v[0];
+}
+
+// Lanes holding the same head differ only in the bits >= GH (token within the group, group).
+template <int GH>
+__device__ __forceinline__ float max_over_tokens(float x) {
+#pragma unroll
+  for (int m = GH; m < 32; m <<= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, m));
+  return x;
+}
+
+template <int GH>
+__device__ __forceinline__ float sum_over_tokens(float x) {
+#pragma unroll
+  for (int m = GH; m < 32; m <<= 1) x += __shfl_xor_sync(kFullMask, x, m);
+  return x;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The decode kernel
+// ---------------------------------------------------------------------------------------------
+
+template <int D, int GH>
+__global__ void __maxnreg__(200)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using T = Traits<D, GH>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* tiles = smem + T::kOffTiles;
+  uint8_t* qbuf = smem + T::kOffQ;
+  float* cb = reinterpret_cast<float*>(smem + T::kOffCb);
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + T::kOffMeta);
+  const uint32_t full0 = smem_addr(smem + T::kOffBar);
+  const uint32_t empty0 = full0 + T::kStages * 8;
+  const uint32_t cmb0 = empty0 + T::kStages * 8;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, T::kWarps);
+    }
+    mbar_init(cmb0, T::kWarps);
+    mbar_init(cmb0 + 8, T::kWarps);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == T::kWarps) {
+    // =============================== producer warp ===============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+    }
+    const uint32_t total = p.header[1] * (uint32_t)p.head_groups;
+    const int split = (int)p.header[2];
+    const int bs = p.block_size;
+    const int box_t = bs < T::kTileT ? bs : T::kTileT;
+    const int nsub = T::kTileT / box_t;
+    const int ent_per_tile = (T::kTileT + bs - 1) / bs;
+    uint32_t issue = 0;
+    bool ok = true;
+    int win_b = -1, win_base = 0, win_val = -1;
+
+    auto claim = [&]() -> uint32_t {
+      uint32_t c = 0;
+      if (lane == 0) c = atomicAdd(p.header, 1u);
+      return __shfl_sync(kFullMask, c, 0);
+    };
+    // Wait until consumers have released the stage slot about to be reused.
+    auto acquire = [&](int stage) -> bool {
+      int good = 1;
+      if (lane == 0)
+        good = mbar_wait(empty0 + 8 * stage, ((issue / T::kStages) & 1) ^ 1) ? 1 : 0;
+      return __shfl_sync(kFullMask, good, 0) != 0;
+    };
+
+    uint32_t c = claim();
+    while (ok) {
+      const int stage = issue % T::kStages;
+      if (c >= total) {
+        ok = acquire(stage);
+        if (ok && lane == 0) {
+          meta[stage].flags = kMetaDone;
+          mbar_arrive(full0 + 8 * stage);
+        }
+        ++issue;
+        break;
+      }
+      const int2 it = p.items[c / (uint32_t)p.head_groups];
+      const int x = (int)(c % (uint32_t)p.head_groups);
+      const uint32_t c_next = claim();
+      const int b = it.x, s = it.y;
+      int ctx = p.context_lens[b];
+      ctx = ctx < p.cap_tokens ? ctx : p.cap_tokens;
+      if (ctx <= 0) {
+        ok = acquire(stage);
+        if (ok && lane == 0) {
+          StageMeta m;
+          m.b = b; m.x = x; m.split = 0; m.nsplit = 1;
+          m.tok0 = 0; m.tok_end = 0; m.flags = kMetaZero; m.pad = 0;
+          meta[stage] = m;
+          mbar_arrive(full0 + 8 * stage);
+        }
+        ++issue;
+        c = c_next;
+        continue;
+      }
+      const int nsplit = (ctx + split - 1) / split;
+      const int tok_begin = s * split;
+      const int tok_end = min(ctx, tok_begin + split);
+      const int need_ent = (ctx + bs - 1) / bs;  // table entries of the whole sequence
+      const int32_t* bt_row = p.block_tables + (int64_t)b * p.max_blocks;
+      const uint16_t* qsrc = p.q + ((int64_t)b * p.num_q_heads + x * GH) * D;
+      const int kv_head = x / p.groups_per_kv;
+
+      for (int tok0 = tok_begin; tok0 < tok_end && ok; tok0 += T::kTileT) {
+        const int st = issue % T::kStages;
+        const int e0 = tok0 / bs;
+        if (win_b != b || e0 < win_base || e0 + ent_per_tile > win_base + 32) {
+          win_b = b;
+          win_base = e0;
+          const int e = e0 + lane;
+          win_val = e < need_ent ? __ldg(bt_row + e) : -1;
+        }
+        int rows[T::kMaxSub];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int sb = 0; sb < T::kMaxSub; ++sb) {
+          rows[sb] = -1;
+          if (sb < nsub) {
+            const int t = tok0 + sb * box_t;
+            const int blk = __shfl_sync(kFullMask, win_val, (t / bs - win_base) & 31);
+            if (t < tok_end) {
+              if (blk >= 0 && blk < p.num_blocks) {
+                rows[sb] = blk * bs + (t & (bs - 1));
+                bytes += 2u * (uint32_t)box_t * T::kRowBytes;
+              } else if (lane == 0) {
+                raise_flag(p.flags, PKV_DEVERR_BAD_BLOCK);
+              }
+            }
+          }
+        }
+        const bool first = tok0 == tok_begin;
+        if (first) bytes += T::kQBytes;
+        ok = acquire(st);
+        if (ok && lane == 0) {
+          StageMeta m;
+          m.b = b; m.x = x; m.split = s; m.nsplit = nsplit;
+          m.tok0 = tok0; m.tok_end = tok_end;
+          m.flags = (first ? kMetaFirst : 0) | (tok0 + T::kTileT >= tok_end ? kMetaLast : 0);
+          m.pad = 0;
+          meta[st] = m;
+          const uint32_t fb = full0 + 8 * st;
+          mbar_arrive_expect_tx(fb, bytes);
+          uint8_t* kdst = tiles + st * T::kStageBytes;
+          uint8_t* vdst = kdst + T::kTileBytes;
+#pragma unroll
+          for (int sb = 0; sb < T::kMaxSub; ++sb) {
+            if (sb < nsub && rows[sb] >= 0) {
+              const int off = sb * box_t * T::kRowBytes;
+              tma_load_3d(smem_addr(kdst + off), &tmap_k, 0, kv_head, rows[sb], fb);
+              tma_load_3d(smem_addr(vdst + off), &tmap_v, 0, kv_head, rows[sb], fb);
+            }
+          }
+          if (first) bulk_load(smem_addr(qbuf + st * T::kQBytes), qsrc, T::kQBytes, fb);
+        }
+        ++issue;
+      }
+      c = c_next;
+    }
+    if (!ok && lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+    // Drain: never leave while a copy into this CTA's shared memory may be in flight.
+    if (lane == 0) {
+      const uint32_t n = issue < (uint32_t)T::kStages ? issue : (uint32_t)T::kStages;
+      for (uint32_t i = issue - n; i < issue; ++i) {
+        if (!mbar_wait(full0 + 8 * (i % T::kStages), (i / T::kStages) & 1)) {
+          raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ================================= consumer warps =================================
+  const int g = lane >> 3;  // lane group: tokens [g*TPG, (g+1)*TPG) of this warp's share
+  const int j = lane & 7;   // dims [(j + 8c) * 8, +8) for chunk c
+  const int my_h = j % GH;  // after the reduce-scatter this lane holds pair (j / GH, j % GH)
+  const int my_t = j / GH;
+  const int tbase = warp * T::kTokPerWarp + g * T::kTPG;
+
+  uint64_t qp[GH][T::kPairs];
+  uint64_t acc[GH][T::kPairs];
+  float m_ref[GH];
+  float l_lane = 0.f;
+  uint32_t use = 0;
+  uint32_t item = 0;
+
+  while (true) {
+    const int st = use % T::kStages;
+    if (!mbar_wait(full0 + 8 * st, (use / T::kStages) & 1)) {
+      if (lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+      return;
+    }
+    const StageMeta mt = meta[st];
+    if (mt.flags & kMetaDone) break;
+
+    if (mt.flags & (kMetaFirst | kMetaZero)) {
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        m_ref[h] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < T::kPairs; ++i) acc[h][i] = 0ull;
+      }
+      l_lane = 0.f;
+    }
+    if (mt.flags & kMetaFirst) {
+      const uint8_t* qs = qbuf + st * T::kQBytes;
+      const uint64_t sc2 = pack2(p.qk_scale_log2, p.qk_scale_log2);
+#pragma unroll
+      for (int h = 0; h < GH; ++h)
+#pragma unroll
+        for (int c = 0; c < T::kChunks; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qs + (h * D + (j + 8 * c) * 8) * 2);
+          qp[h][4 * c + 0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
+          qp[h][4 * c + 1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
+          qp[h][4 * c + 2] = fmul2(bf16x2_to_f32x2(w.z), sc2);
+          qp[h][4 * c + 3] = fmul2(bf16x2_to_f32x2(w.w), sc2);
+        }
+    }
+
+    if (!(mt.flags & kMetaZero)) {
+      const uint8_t* kt = tiles + st * T::kStageBytes;
+      const uint8_t* vt = kt + T::kTileBytes;
+      const int n_valid = mt.tok_end - mt.tok0;  // tokens of this tile that count (may exceed)
+
+      // ---- scores: partial q.k over this lane's dims for its TPG tokens x GH heads ----
+      float part[8];
+#pragma unroll
+      for (int tt = 0; tt < T::kTPG; ++tt) {
+        const uint8_t* row = kt + (tbase + tt) * T::kRowBytes;
+        uint64_t s2[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) s2[h] = 0ull;
+#pragma unroll
+        for (int c = 0; c < T::kChunks; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + (j + 8 * c) * 16);
+          const uint64_t k0 = bf16x2_to_f32x2(w.x), k1 = bf16x2_to_f32x2(w.y);
+          const uint64_t k2 = bf16x2_to_f32x2(w.z), k3 = bf16x2_to_f32x2(w.w);
+#pragma unroll
+          for (int h = 0; h < GH; ++h) {
+            s2[h] = ffma2(qp[h][4 * c + 0], k0, s2[h]);
+            s2[h] = ffma2(qp[h][4 * c + 1], k1, s2[h]);
+            s2[h] = ffma2(qp[h][4 * c + 2], k2, s2[h]);
+            s2[h] = ffma2(qp[h][4 * c + 3], k3, s2[h]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          const float2 f = unpack2(s2[h]);
+          part[tt * GH + h] = f.x + f.y;
+        }
+      }
+      float sc = reduce_scatter8(part, j);
+      const bool valid = (tbase + my_t) < n_valid;
+      sc = valid ? sc : -INFINITY;
+
+      // ---- online softmax (log2 units), lazy rescale ----
+      const float mx = max_over_tokens<GH>(sc);
+      float mt_all[GH];
+#pragma unroll
+      for (int h = 0; h < GH; ++h) mt_all[h] = __shfl_sync(kFullMask, mx, h);
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < GH; ++h) need |= mt_all[h] > m_ref[h] + kTau;
+      if (need) {
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          if (mt_all[h] > m_ref[h] + kTau) {
+            const float alpha = fast_exp2(m_ref[h] - mt_all[h]);
+            const uint64_t a2 = pack2(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < T::kPairs; ++i) acc[h][i] = fmul2(acc[h][i], a2);
+            if (my_h == h) l_lane *= alpha;
+            m_ref[h] = mt_all[h];
+          }
+        }
+      }
+      float my_m = m_ref[0];
+#pragma unroll
+      for (int h = 1; h < GH; ++h)
+        if (my_h == h) my_m = m_ref[h];
+      const float pr = valid ? fast_exp2(sc - my_m) : 0.f;
+      l_lane += pr;
+
+      // ---- acc += p * V over this lane group's tokens ----
+#pragma unroll
+      for (int tt = 0; tt < T::kTPG; ++tt) {
+        uint64_t pp[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          const float pv = __shfl_sync(kFullMask, pr, (lane & ~7) | (tt * GH + h));
+          pp[h] = pack2(pv, pv);
+        }
+        const bool tok_ok = (tbase + tt) < n_valid;
+        const uint8_t* row = vt + (tbase + tt) * T::kRowBytes;
+#pragma unroll
+        for (int c = 0; c < T::kChunks; ++c) {
+          uint4 w = *reinterpret_cast<const uint4*>(row + (j + 8 * c) * 16);
+          if (!tok_ok) w = make_uint4(0u, 0u, 0u, 0u);  // stale shared memory past the end
+          const uint64_t v0 = bf16x2_to_f32x2(w.x), v1 = bf16x2_to_f32x2(w.y);
+          const uint64_t v2 = bf16x2_to_f32x2(w.z), v3 = bf16x2_to_f32x2(w.w);
+#pragma unroll
+          for (int h = 0; h < GH; ++h) {
+            acc[h][4 * c + 0] = ffma2(pp[h], v0, acc[h][4 * c + 0]);
+            acc[h][4 * c + 1] = ffma2(pp[h], v1, acc[h][4 * c + 1]);
+            acc[h][4 * c + 2] = ffma2(pp[h], v2, acc[h][4 * c + 2]);
+            acc[h][4 * c + 3] = ffma2(pp[h], v3, acc[h][4 * c + 3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    ++use;
+
+    if (!(mt.flags & (kMetaLast | kMetaZero))) continue;
+
+    // ---- item finished: merge the lane groups, then the warps, then write ----
+#pragma unroll
+    for (int h = 0; h < GH; ++h)
+#pragma unroll
+      for (int i = 0; i < T::kPairs; ++i) {
+        float2 v = unpack2(acc[h][i]);
+        v.x += __shfl_xor_sync(kFullMask, v.x, 8);
+        v.y += __shfl_xor_sync(kFullMask, v.y, 8);
+        v.x += __shfl_xor_sync(kFullMask, v.x, 16);
+        v.y += __shfl_xor_sync(kFullMask, v.y, 16);
+        acc[h][i] = pack2(v.x, v.y);
+      }
+    const float l_warp = sum_over_tokens<GH>(l_lane);  // lane h now holds head h's sum
+    const int par = item & 1;
+    float* cbw = cb + (par * T::kWarps + warp) * T::kCbFloats;
+    if (g == 0) {
+#pragma unroll
+      for (int h = 0; h < GH; ++h)
+#pragma unroll
+        for (int c = 0; c < T::kChunks; ++c) {
+          float* dst = cbw + h * D + (j + 8 * c) * 8;
+          const float2 a0 = unpack2(acc[h][4 * c + 0]), a1 = unpack2(acc[h][4 * c + 1]);
+          const float2 a2 = unpack2(acc[h][4 * c + 2]), a3 = unpack2(acc[h][4 * c + 3]);
+          reinterpret_cast<float4*>(dst)[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+        }
+    }
+    if (lane < GH) {
+      float mm = m_ref[0];
+#pragma unroll
+      for (int h = 1; h < GH; ++h)
+        if (lane == h) mm = m_ref[h];
+      cbw[GH * D + lane] = mm;
+      cbw[GH * D + GH + lane] = l_warp;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cmb0 + 8 * par);
+    if (!mbar_wait(cmb0 + 8 * par, (item >> 1) & 1)) {
+      if (lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+      return;
+    }
+    const float* cbp = cb + par * T::kWarps * T::kCbFloats;
+    const bool final_out = mt.nsplit == 1;
+    // Warp w writes outputs o = 64 w + 2 lane + 256 k: one (head, 64-dim slice) per k.
+    for (int o = 64 * warp + 2 * lane; o < GH * D; o += T::kWarps * 64) {
+      const int h = o / D, d = o % D;
+      float mw[T::kWarps];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < T::kWarps; ++w) {
+        mw[w] = cbp[w * T::kCbFloats + GH * D + h];
+        M = fmaxf(M, mw[w]);
+      }
+      float den = 0.f, n0 = 0.f, n1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < T::kWarps; ++w) {
+        const float wt = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
+        den += wt * cbp[w * T::kCbFloats + GH * D + GH + h];
+        const float2 a = *reinterpret_cast<const float2*>(cbp + w * T::kCbFloats + h * D + d);
+        n0 += wt * a.x;
+        n1 += wt * a.y;
+      }
+      const int head = mt.x * GH + h;
+      if (final_out) {
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)mt.b * p.num_q_heads + head) * D +
+                                           d) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
+      } else {
+        const int64_t pi = ((int64_t)mt.b * p.max_splits + mt.split) * p.num_q_heads + head;
+        *reinterpret_cast<float2*>(p.part_acc + pi * D + d) = make_float2(n0, n1);
+        if (lane == 0) p.part_ml[pi * (D / 64) + d / 64] = make_float2(M, den);
+      }
+    }
+    if (!final_out) {
+      // Chunk partials are out; the warp that finishes last for this (sequence, head group,
+      // slice) merges all chunks: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
+      __threadfence();
+      __syncwarp();
+      uint32_t done = 0;
+      if (lane == 0)
+        done = atomicAdd(p.counters + ((int64_t)mt.b * p.head_groups + mt.x) * T::kWarps + warp,
+                         1u);
+      done = __shfl_sync(kFullMask, done, 0);
+      if (done == (uint32_t)mt.nsplit - 1) {
+        __threadfence();
+        for (int o = 64 * warp + 2 * lane; o < GH * D; o += T::kWarps * 64) {
+          const int h = o / D, d = o % D;
+          const int head = mt.x * GH + h;
+          const int64_t base = (int64_t)mt.b * p.max_splits * p.num_q_heads + head;
+          float M = -INFINITY;
+          for (int sp = 0; sp < mt.nsplit; ++sp)
+            M = fmaxf(M, __ldcg(p.part_ml + (base + (int64_t)sp * p.num_q_heads) * (D / 64) +
+                                d / 64).x);
+          float den = 0.f, n0 = 0.f, n1 = 0.f;
+          for (int sp = 0; sp < mt.nsplit; ++sp) {
+            const int64_t pi = base + (int64_t)sp * p.num_q_heads;
+            const float2 ml = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
+            const float wt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+            den += wt * ml.y;
+            const float2 a = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
+            n0 += wt * a.x;
+            n1 += wt * a.y;
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)mt.b * p.num_q_heads + head) *
+                                                         D + d) =
+              __floats2bfloat162_rn(n0 * inv, n1 * inv);
+        }
+      }
+    }
+    ++item;
+  }
+}
+
+template <int D, int GH>
+cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int num_sms, cudaStream_t stream) {
+  using T = Traits<D, GH>;
+  static int ctas_per_sm = 0;  // per process; all B300s alike
+  if (ctas_per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, GH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, GH>,
+                                                      T::kThreads, T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    ctas_per_sm = n < 1 ? 1 : n;
+  }
+  const int G = a.num_q_heads / a.cache.num_kv_heads;
+  DecodeParams p;
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.out = a.out;
+  p.part_acc = a.ws.part_acc;
+  p.part_ml = a.ws.part_ml;
+  p.items = a.ws.items;
+  p.header = a.ws.header;
+  p.counters = a.ws.counters;
+  p.flags = a.flags;
+  p.max_blocks = a.max_blocks;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.head_groups = a.num_q_heads / GH;
+  p.groups_per_kv = G / GH;
+  p.block_size = a.cache.block_size;
+  p.num_blocks = a.cache.num_blocks;
+  p.max_splits = a.max_splits;
+  const int64_t cap_table = (int64_t)a.max_blocks * a.cache.block_size;
+  const int64_t cap_plan = (int64_t)a.max_splits * a.split_tokens;
+  int64_t cap = cap_table < cap_plan ? cap_table : cap_plan;
+  if (cap > 0x7fffffff) cap = 0x7fffffff;
+  p.cap_tokens = (int32_t)cap;
+  p.qk_scale_log2 = a.scale * 1.4426950408889634f;
+
+  const int64_t upper = (int64_t)a.num_seqs * a.max_splits * p.head_groups;
+  int64_t grid = (int64_t)num_sms * ctas_per_sm;
+  if (grid > upper) grid = upper;
+  if (grid < 1) grid = 1;
+
+  PlanParams pp;
+  pp.context_lens = a.context_lens;
+  pp.items = a.ws.items;
+  pp.header = a.ws.header;
+  pp.counters = a.ws.counters;
+  pp.flags = a.flags;
+  pp.num_seqs = a.num_seqs;
+  pp.cap_tokens = p.cap_tokens;
+  pp.split_floor = a.split_tokens;
+  pp.fixed_split = a.auto_split ? 0 : a.split_tokens;
+  pp.head_groups = p.head_groups;
+  pp.slots = (int32_t)((int64_t)num_sms * ctas_per_sm);
+  pp.num_counters = a.max_splits > 1 ? a.num_seqs * p.head_groups * T::kWarps : 0;
+  decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  paged_decode_kernel<D, GH><<<(unsigned)grid, T::kThreads, T::kSmemBytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                              int32_t max_splits, DecodeWorkspace* carve, void* base) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t n_items = (size_t)num_seqs * max_splits;
+  size_t off = 0;
+  const size_t header = off;
+  off += 256;
+  const size_t items = off;
+  off += up(n_items * sizeof(int2));
+  size_t counters = 0, acc = 0, ml = 0;
+  if (max_splits > 1) {
+    // one counter per (sequence, query head, consumer warp) bounds every head grouping
+    counters = off;
+    off += up((size_t)num_seqs * num_q_heads * 4 * sizeof(uint32_t));
+    acc = off;
+    off += up(n_items * num_q_heads * head_dim * sizeof(float));
+    ml = off;
+    off += up(n_items * num_q_heads * (head_dim / 64) * sizeof(float2));
+  }
+  if (carve != nullptr) {
+    uint8_t* b8 = static_cast<uint8_t*>(base);
+    carve->header = reinterpret_cast<uint32_t*>(b8 + header);
+    carve->items = reinterpret_cast<int2*>(b8 + items);
+    carve->counters = max_splits > 1 ? reinterpret_cast<uint32_t*>(b8 + counters) : nullptr;
+    carve->part_acc = max_splits > 1 ? reinterpret_cast<float*>(b8 + acc) : nullptr;
+    carve->part_ml = max_splits > 1 ? reinterpret_cast<float2*>(b8 + ml) : nullptr;
+  }
+  return off;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                int num_sms, cudaStream_t stream) {
+  const int G = a.num_q_heads / a.cache.num_kv_heads;
+  const int GH = G >= 4 ? 4 : G;
+  if (a.cache.head_dim == 128) {
+    if (GH == 4) return launch_instance<128, 4>(a, tk, tv, num_sms, stream);
+    if (GH == 2) return launch_instance<128, 2>(a, tk, tv, num_sms, stream);
+    if (GH == 1) return launch_instance<128, 1>(a, tk, tv, num_sms, stream);
+  } else if (a.cache.head_dim == 64) {
+    if (GH == 4) return launch_instance<64, 4>(a, tk, tv, num_sms, stream);
+    if (GH == 2) return launch_instance<64, 2>(a, tk, tv, num_sms, stream);
+    if (GH == 1) return launch_instance<64, 1>(a, tk, tv, num_sms, stream);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

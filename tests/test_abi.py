@@ -1,0 +1,136 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol the header declares, and its
+host-side logic (decode plan, argument validation) behaves as documented. No kernel is launched:
+every call here fails validation (or is a no-op) before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import paged_kv_cache_496_b300 as pk
+    return pk
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+
+
+def test_header_declares_the_three_operations():
+    names = declared_symbols()
+    for n in ("pkv_kv_store", "pkv_paged_decode", "pkv_paged_prefill", "pkv_decode_plan_make",
+              "pkv_get_device_error", "pkv_status_string", "pkv_last_error", "pkv_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    out = subprocess.run(["nm", "-D", "--defined-only", pk.LIBRARY], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(pkv_\w+)", out))
+    for n in declared_symbols():
+        assert n in exported, f"{n} not exported"
+        assert getattr(pk.lib, n) is not None
+
+
+def test_status_strings_and_version(pk):
+    assert pk.lib.pkv_version() >= 100
+    assert pk.lib.pkv_status_string(0) == b"ok"
+    assert pk.lib.pkv_status_string(-3) == b"workspace too small"
+    assert pk.lib.pkv_status_string(12345) == b"unknown status"
+
+
+def _desc(pk, nb=64, bs=16, hkv=8, d=128):
+    return pk.CacheDesc(nb, bs, hkv, d)
+
+
+def test_decode_plan_no_split_for_short_contexts(pk):
+    plan = pk.DecodePlan()
+    assert pk.lib.pkv_decode_plan_make(1024, 32, _desc(pk, 5000, 256), 400, 0,
+                                       ctypes.byref(plan)) == 0
+    assert plan.max_splits == 1 and plan.auto_split == 0 and plan.split_tokens == 512
+    assert plan.workspace_bytes >= 256 + 1024 * 8
+
+
+def test_decode_plan_auto_and_fixed(pk):
+    plan = pk.DecodePlan()
+    assert pk.lib.pkv_decode_plan_make(64, 32, _desc(pk, 9000, 16), 32768, 0,
+                                       ctypes.byref(plan)) == 0
+    assert plan.auto_split == 1 and plan.split_tokens == 512 and plan.max_splits == 64
+    # partials: [B, splits, Hq, D] fp32 + (m, l) per 64-dim slice + counters + items + header
+    assert plan.workspace_bytes >= 64 * 64 * 32 * 128 * 4
+    assert pk.lib.pkv_decode_plan_make(64, 32, _desc(pk, 9000, 16), 32768, 1000,
+                                       ctypes.byref(plan)) == 0
+    assert plan.auto_split == 0 and plan.split_tokens == 1024 and plan.max_splits == 32
+    assert pk.lib.pkv_decode_plan_make(64, 32, _desc(pk, 9000, 16), 32768, -1,
+                                       ctypes.byref(plan)) == 0
+    assert plan.max_splits == 1 and plan.split_tokens == 32768
+
+
+@pytest.mark.parametrize("desc,hq,status", [
+    ((64, 16, 8, 96), 32, -2),    # head_dim 96 unsupported
+    ((64, 24, 8, 128), 32, -2),   # block size not a power of two
+    ((64, 512, 8, 128), 32, -2),  # block size above 256
+    ((64, 16, 8, 128), 12, -1),   # Hq not a multiple of Hkv
+    ((64, 16, 2, 128), 32, -2),   # group size 16 unsupported
+    ((0, 16, 8, 128), 32, -1),    # empty pool
+])
+def test_decode_plan_rejects_shapes(pk, desc, hq, status):
+    plan = pk.DecodePlan()
+    assert pk.lib.pkv_decode_plan_make(4, hq, pk.CacheDesc(*desc), 100, 0,
+                                       ctypes.byref(plan)) == status
+    assert pk.lib.pkv_last_error() != b""
+
+
+def test_kv_store_validation_without_launch(pk):
+    d = _desc(pk)
+    assert pk.lib.pkv_kv_store(None, None, None, 0, None, None, d, None) == 0  # no-op
+    assert pk.lib.pkv_kv_store(None, None, None, 5, None, None, d, None) == -1
+    assert pk.lib.pkv_kv_store(256, 256, 256, -1, 256, 256, d, None) == -1
+    assert pk.lib.pkv_kv_store(256, 256, 256, 5, 264, 256, d, None) == -1  # misaligned cache
+    assert pk.lib.pkv_kv_store(256, 256, 256, 5, 256, 256, _desc(pk, d=80), None) == -2
+
+
+def test_decode_validation_without_launch(pk):
+    d = _desc(pk)
+    plan = pk.DecodePlan()
+    assert pk.lib.pkv_decode_plan_make(4, 32, d, 100, 0, ctypes.byref(plan)) == 0
+    args = dict(q=256, kc=256, vc=256, bt=256, mb=8, cl=256, B=4, Hq=32, scale=0.1,
+                out=256, ws=4096, wsb=plan.workspace_bytes)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return pk.lib.pkv_paged_decode(a["q"], a["kc"], a["vc"], d, a["bt"], a["mb"], a["cl"],
+                                       a["B"], a["Hq"], a["scale"], ctypes.byref(plan),
+                                       a["out"], a["ws"], a["wsb"], None)
+
+    assert call(B=0) == 0                       # empty batch: no-op
+    assert call(q=None) == -1                   # null pointer
+    assert call(ws=4096 + 16) == -1             # workspace not 256-byte aligned
+    assert call(mb=0) == -1                     # empty block table rows
+    assert call(scale=float("nan")) == -1       # non-finite scale
+    assert call(wsb=plan.workspace_bytes - 1) == -3
+    assert b"workspace" in pk.lib.pkv_last_error()
+    assert call(Hq=12) == -1
+
+
+def test_prefill_validation_without_launch(pk):
+    d = _desc(pk)
+    assert pk.lib.pkv_paged_prefill(None, None, None, None, None, 0, 0, 0, None, 0, None, None,
+                                    d, 32, 0.1, None, None) in (0, -2)
+    assert pk.lib.pkv_paged_prefill(None, 256, 256, 256, 256, 2, 10, 5, None, 0, None, None,
+                                    d, 32, 0.1, 256, None) in (-1, -2)
+
+
+def test_binding_refuses_cpu_tensors(pk):
+    import torch
+    k = torch.zeros(4, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pk.kv_store(k, k, torch.zeros(4, dtype=torch.int32), torch.zeros(2, 16, 8, 128,
+                    dtype=torch.bfloat16), torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16))

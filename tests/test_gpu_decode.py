@@ -1,0 +1,311 @@
+"""GPU parity: kv_store and paged_decode through the C ABI against the fp64 CPU oracle.
+
+Bars: the cache after kv_store is bit-exact; attention outputs are within max-abs 2e-2 of the
+oracle (N(0,1) inputs), and exactly bf16(V0) when the context is one token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_496_b300 as pk
+import workloads as W
+from tests.gpu_util import (TOL, DeviceDecodeLayer, assert_attn_close, dev_bf16, dev_i32,
+                            host_bits, oracle_decode_from_snapshot)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pk.get_device_error()  # clear
+    yield
+    assert pk.get_device_error() == 0
+
+
+def _upload(case: W.DecodeCase):
+    return dict(kc=dev_bf16(case.k_cache), vc=dev_bf16(case.v_cache), k=dev_bf16(case.k_new),
+                v=dev_bf16(case.v_new), slots=dev_i32(case.slot_mapping), q=dev_bf16(case.q),
+                bt=dev_i32(case.block_tables), ctx=dev_i32(case.context_lens))
+
+
+# ------------------------------------------------------------------------------------------------
+# KV store
+# ------------------------------------------------------------------------------------------------
+
+
+def test_store_tiny_bit_exact(orc):
+    case = W.tiny_decode_case()
+    d = _upload(case)
+    pk.kv_store(d["k"], d["v"], d["slots"], d["kc"], d["vc"])
+    rk, rv, bad = orc.kv_store(case.k_new, case.v_new, case.slot_mapping, case.k_cache,
+                               case.v_cache)
+    assert bad == 0
+    assert np.array_equal(host_bits(d["kc"]), rk) and np.array_equal(host_bits(d["vc"]), rv)
+
+
+@pytest.mark.parametrize("Hkv,D,BS", [(8, 128, 256), (2, 64, 16), (1, 64, 32), (4, 128, 64)])
+def test_store_padding_sentinel_and_bad_slots(orc, Hkv, D, BS):
+    rng = W.rng_for(77, Hkv, D)
+    T = 300
+    NB = -(-T // BS) + 3
+    sentinel = np.full((NB, BS, Hkv, D), 0x7FC1, np.uint16)
+    slots = rng.permutation(NB * BS)[:T].astype(np.int32)
+    slots[rng.random(T) < 0.2] = -1
+    k = W.normal_bf16(rng, (T, Hkv, D))
+    v = W.normal_bf16(rng, (T, Hkv, D))
+    kc, vc = dev_bf16(sentinel), dev_bf16(sentinel)
+    pk.kv_store(dev_bf16(k), dev_bf16(v), dev_i32(slots), kc, vc)
+    rk, rv, _ = orc.kv_store(k, v, slots, sentinel, sentinel)
+    assert np.array_equal(host_bits(kc), rk) and np.array_equal(host_bits(vc), rv)
+    assert pk.get_device_error() == 0
+    # out-of-range and negative slots other than -1 are skipped and flagged, never written
+    bad = slots.copy()
+    bad[0], bad[1] = NB * BS, -7
+    kc2, vc2 = dev_bf16(sentinel), dev_bf16(sentinel)
+    pk.kv_store(dev_bf16(k), dev_bf16(v), dev_i32(bad), kc2, vc2)
+    rk2, _, nbad = orc.kv_store(k, v, bad, sentinel, sentinel)
+    assert nbad == 2 and np.array_equal(host_bits(kc2), rk2)
+    assert pk.get_device_error() == pk.DEVERR_BAD_SLOT
+
+
+def test_store_empty_is_noop():
+    kc = torch.zeros((2, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    e = torch.zeros((0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    pk.kv_store(e, e, torch.zeros(0, dtype=torch.int32, device="cuda"), kc, kc.clone())
+    assert torch.count_nonzero(kc) == 0
+
+
+# ------------------------------------------------------------------------------------------------
+# Decode, small cases against the oracle
+# ------------------------------------------------------------------------------------------------
+
+
+def _run_decode(case, split_tokens=0):
+    d = _upload(case)
+    pk.kv_store(d["k"], d["v"], d["slots"], d["kc"], d["vc"])
+    out = pk.paged_decode(d["q"], d["kc"], d["vc"], d["bt"], d["ctx"], case.scale,
+                          max_context_len=case.max_context_len, split_tokens=split_tokens)
+    assert pk.get_device_error() == 0
+    return out, d
+
+
+def _oracle_decode(orc, case):
+    kc, vc, _ = orc.kv_store(case.k_new, case.v_new, case.slot_mapping, case.k_cache,
+                             case.v_cache)
+    return orc.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale)
+
+
+def test_decode_tiny_config(orc):
+    case = W.tiny_decode_case()
+    out, _ = _run_decode(case)
+    assert_attn_close(out, _oracle_decode(orc, case), what="tiny decode")
+
+
+SHAPES = [  # (B, Hq, Hkv, D, BS, ctx_lo, ctx_hi)
+    (5, 4, 2, 64, 16, 1, 64),
+    (7, 8, 8, 128, 16, 1, 300),     # G = 1
+    (6, 16, 8, 128, 256, 100, 700),  # G = 2 (Qwen3-0.6B heads)
+    (6, 32, 8, 128, 256, 100, 900),  # G = 4 (Qwen3-8B heads)
+    (4, 64, 8, 128, 32, 1, 500),     # G = 8 (two CTAs of four heads per kv head)
+    (5, 8, 2, 64, 64, 30, 260),      # D = 64, G = 4
+    (3, 4, 4, 64, 128, 1, 140),      # D = 64, G = 1
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%d_H%d-%d_D%d_BS%d" % s[:5])
+@pytest.mark.parametrize("q_scale", [1.0, 8.0], ids=["normal", "sharp"])
+def test_decode_shapes(orc, shape, q_scale):
+    B, Hq, Hkv, D, BS, lo, hi = shape
+    case = W.random_decode_case(1000 + B + Hq + D + BS, B, Hq, Hkv, D, BS, lo, hi, extra_pool=3,
+                                pad_slots=2, q_scale=q_scale)
+    out, _ = _run_decode(case)
+    assert_attn_close(out, _oracle_decode(orc, case), what=f"decode {shape}")
+
+
+def test_decode_ragged_edges(orc):
+    """Context lengths at and around tile and block boundaries, and a single token."""
+    ctx = np.array([1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511,
+                    512, 513], np.int32)
+    for Hq, BS in ((32, 16), (16, 256), (8, 64)):
+        case = W.random_decode_case(2024 + Hq, len(ctx), Hq, 8, 128, BS, 0, 0,
+                                    context_lens=ctx)
+        out, _ = _run_decode(case)
+        assert_attn_close(out, _oracle_decode(orc, case), what=f"ragged Hq={Hq} BS={BS}")
+
+
+def test_decode_single_token_is_exact():
+    """ctx = 1: the output is the value row itself, so bf16(V0) exactly."""
+    case = W.random_decode_case(5, 6, 32, 8, 128, 16, 1, 1)
+    out, d = _run_decode(case)
+    G = 4
+    for b in range(case.num_seqs):
+        blk = case.block_tables[b, 0]
+        v0 = host_bits(d["vc"])[blk, 0]  # written by kv_store at position 0
+        assert np.array_equal(host_bits(out[b]), np.repeat(v0, G, axis=0))
+
+
+@pytest.mark.parametrize("split", [128, 256, 512, -1, 0])
+def test_decode_split_matches_oracle(orc, split):
+    case = W.random_decode_case(31, 6, 32, 8, 128, 16, 1, 3000)
+    out, _ = _run_decode(case, split_tokens=split)
+    assert_attn_close(out, _oracle_decode(orc, case), what=f"split={split}")
+
+
+def test_decode_split_agrees_with_unsplit():
+    case = W.random_decode_case(32, 5, 16, 8, 128, 64, 600, 2500)
+    a, _ = _run_decode(case, split_tokens=-1)
+    b, _ = _run_decode(case, split_tokens=256)
+    assert (a.float() - b.float()).abs().max().item() <= TOL
+
+
+def test_decode_zero_context_rows_are_zero(orc):
+    """Padded batch entries (context 0, slot -1) produce zeros and do not disturb the others."""
+    ctx = np.array([300, 0, 17, 0, 1, 999], np.int32)
+    case = W.random_decode_case(33, len(ctx), 32, 8, 128, 16, 0, 0, context_lens=ctx,
+                                pad_slots=2)
+    for split in (0, 128, -1):
+        out, _ = _run_decode(case, split_tokens=split)
+        ref = _oracle_decode(orc, case)
+        assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[3]) == 0
+        assert_attn_close(out, ref, what=f"zero-context rows split={split}")
+
+
+def test_decode_placement_invariance():
+    """Permuting physical blocks (tables permuted alike) gives bit-identical outputs."""
+    case = W.random_decode_case(34, 6, 32, 8, 128, 16, 50, 700)
+    a, _ = _run_decode(case, split_tokens=-1)
+    perm = W.rng_for(34, 7).permutation(case.num_blocks)
+    kc2, vc2 = np.empty_like(case.k_cache), np.empty_like(case.v_cache)
+    kc2[perm], vc2[perm] = case.k_cache, case.v_cache
+    bt2 = np.where(case.block_tables >= 0, perm[np.maximum(case.block_tables, 0)], -1)
+    sl2 = np.where(case.slot_mapping >= 0,
+                   perm[np.maximum(case.slot_mapping, 0) // 16] * 16 + case.slot_mapping % 16, -1)
+    case2 = W.DecodeCase(case.num_blocks, 16, 8, 128, 32, kc2, vc2, case.k_new, case.v_new,
+                         sl2.astype(np.int32), case.q, bt2.astype(np.int32), case.context_lens,
+                         case.scale)
+    b, _ = _run_decode(case2, split_tokens=-1)
+    assert torch.equal(a, b)
+
+
+def test_decode_shared_blocks_equal_copies():
+    """Sequences that share physical blocks give the same result as ones that own copies."""
+    rng = W.rng_for(35, 0)
+    BS, Hkv, D, ctx = 16, 8, 128, 200
+    nb = -(-ctx // BS)
+    kc = W.normal_bf16(rng, (2 * nb, BS, Hkv, D))
+    vc = W.normal_bf16(rng, (2 * nb, BS, Hkv, D))
+    kc[nb:], vc[nb:] = kc[:nb], vc[:nb]
+    q = dev_bf16(W.normal_bf16(rng, (2, 32, D)))
+    cl = dev_i32([ctx, ctx])
+    shared = dev_i32([np.arange(nb), np.arange(nb)])
+    dup = dev_i32([np.arange(nb), np.arange(nb, 2 * nb)])
+    o1 = pk.paged_decode(q, dev_bf16(kc), dev_bf16(vc), shared, cl, 0.088, max_context_len=ctx)
+    o2 = pk.paged_decode(q, dev_bf16(kc), dev_bf16(vc), dup, cl, 0.088, max_context_len=ctx)
+    assert torch.equal(o1, o2)
+
+
+def test_decode_bad_block_id_is_flagged_not_faulted():
+    case = W.random_decode_case(36, 3, 32, 8, 128, 16, 40, 60)
+    d = _upload(case)
+    pk.kv_store(d["k"], d["v"], d["slots"], d["kc"], d["vc"])
+    pk.get_device_error()
+    bt = d["bt"].clone()
+    bt[1, 1] = case.num_blocks + 5  # outside the pool
+    bt[2, 0] = -3
+    pk.paged_decode(d["q"], d["kc"], d["vc"], bt, d["ctx"], case.scale, max_context_len=60)
+    assert pk.get_device_error() & pk.DEVERR_BAD_BLOCK
+
+
+def test_decode_context_beyond_table_is_clamped_and_flagged():
+    case = W.random_decode_case(37, 3, 32, 8, 128, 16, 40, 60)
+    d = _upload(case)
+    pk.get_device_error()
+    ctx = d["ctx"].clone()
+    ctx[0] = case.block_tables.shape[1] * 16 + 100  # longer than its block table row
+    pk.paged_decode(d["q"], d["kc"], d["vc"], d["bt"], ctx, case.scale, max_context_len=2000)
+    assert pk.get_device_error() & pk.DEVERR_CTX_CLAMPED
+
+
+def test_decode_graph_capture_matches_eager():
+    case = W.random_decode_case(38, 8, 32, 8, 128, 16, 10, 1500)
+    d = _upload(case)
+    plan = pk.decode_plan(case.num_seqs, 32, d["kc"], case.max_context_len, 0)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    eager = pk.paged_decode(d["q"], d["kc"], d["vc"], d["bt"], d["ctx"], case.scale,
+                            plan=plan, workspace=ws).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pk.kv_store(d["k"], d["v"], d["slots"], d["kc"], d["vc"])
+            pk.paged_decode(d["q"], d["kc"], d["vc"], d["bt"], d["ctx"], case.scale, out=out,
+                            plan=plan, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    # the captured step also stores the new token, so compare against an eager store + decode
+    ref = pk.paged_decode(d["q"], d["kc"], d["vc"], d["bt"], d["ctx"], case.scale, plan=plan,
+                          workspace=ws)
+    assert torch.equal(out, ref)
+    assert eager.shape == out.shape
+
+
+# ------------------------------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times, sampled against the oracle
+# ------------------------------------------------------------------------------------------------
+
+
+def _full_size(orc, ctx, Hq, Hkv, D, BS, seed, sample, pad_to=0, split=0):
+    layer = DeviceDecodeLayer(ctx, Hq, Hkv, D, BS, seed, pad_to=pad_to)
+    snap = layer.snapshot(sample)
+    pk.kv_store(layer.k_new, layer.v_new, layer.slots_dev, layer.k_cache, layer.v_cache)
+    out = pk.paged_decode(layer.q, layer.k_cache, layer.v_cache, layer.bt_dev, layer.ctx_dev,
+                          layer.scale, max_context_len=int(ctx.max()), split_tokens=split)
+    assert pk.get_device_error() == 0
+    ref, kc_ref, vc_ref = oracle_decode_from_snapshot(orc, snap, layer.scale, Hq)
+    idx = torch.from_numpy(snap["blocks"].astype(np.int64)).cuda()
+    assert np.array_equal(host_bits(layer.k_cache.index_select(0, idx)), kc_ref)
+    assert np.array_equal(host_bits(layer.v_cache.index_select(0, idx)), vc_ref)
+    err = assert_attn_close(out[torch.as_tensor(sample, device="cuda")], ref,
+                            what=f"full-size B={len(ctx)} Hq={Hq} BS={BS}")
+    assert torch.isfinite(out.float()).all()
+    return err
+
+
+@pytest.mark.slow
+def test_full_qwen3_8b_decode_layer(orc):
+    ctx = W.decode_lengths("qwen3_8b_decode")
+    rng = W.rng_for(3, 200)
+    sample = np.concatenate([[int(np.argmax(ctx)), int(np.argmin(ctx))],
+                             rng.choice(len(ctx), 14, replace=False)])
+    _full_size(orc, ctx, 32, 8, 128, 256, 3, sample)
+
+
+@pytest.mark.slow
+def test_full_qwen3_8b_live_batch_with_ladder_padding(orc):
+    """A live batch below 1024 padded to the CUDA-graph ladder: padded rows have context 0."""
+    n = W.live_batch_size("qwen3_8b_decode")
+    live = W.decode_lengths("qwen3_8b_decode", live=n)
+    padded = W.ladder_padded_size(n)
+    ctx = np.concatenate([live, np.zeros(padded - n, np.int32)])
+    sample = np.concatenate([np.arange(3), [n - 1, n, padded - 1]])
+    _full_size(orc, ctx, 32, 8, 128, 256, 13, sample, pad_to=padded)
+
+
+@pytest.mark.slow
+def test_full_qwen3_0p6b_decode_layer(orc):
+    ctx = W.decode_lengths("qwen3_0p6b_decode")
+    sample = W.rng_for(2, 200).choice(len(ctx), 16, replace=False)
+    _full_size(orc, ctx, 16, 8, 128, 256, 2, sample)
+
+
+@pytest.mark.slow
+def test_full_long_context_split_decode(orc):
+    ctx = W.decode_lengths("long_splitk_decode")
+    sample = np.concatenate([[0, 3], np.arange(4, 64, 3)])
+    for split in (0, 256):
+        _full_size(orc, ctx, 32, 8, 128, 16, 5, sample, split=split)
