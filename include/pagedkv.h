@@ -135,6 +135,36 @@ PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const u
                      uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Paged decode without any device allocation by the caller (no counterpart in the source pages:
+ * it exists for callers of this library that cannot allocate device memory).
+ * Some callers cannot call cudaMalloc for the decode workspace: a process that has given all of
+ * a GPU's memory to its own pool allocator, or code that must not enter an allocator where it
+ * runs attention (for example a plugin invoked inside another runtime's execution loop). This
+ * entry point computes exactly what pkv_paged_decode computes, with the same arguments minus
+ * workspace and workspace_bytes: its workspace is a fixed array of PKV_STATIC_WS_BYTES (8 MiB)
+ * in the library's own device memory, which every GPU that loads the library holds until the
+ * process exits. It calls no allocating routine.
+ *  - A plan whose workspace_bytes exceeds PKV_STATIC_WS_BYTES is rejected with
+ *    PKV_ERR_WORKSPACE_TOO_SMALL (pkv_last_error() gives both sizes) before anything is enqueued;
+ *    a plan with fewer splits (split_tokens_hint < 0 never splits) needs far less.
+ *  - The first call on each device looks up the array's device address on that device; make
+ *    that first call before any stream capture.
+ *  - All calls on a device share the array, which keeps the previous call's contents; each call
+ *    re-initialises what must start at zero itself. Calls that overlap on the GPU (unordered
+ *    streams) race on the array: order them, e.g. on one stream.
+ * The caller still owns and passes every input and the output.
+ */
+#define PKV_STATIC_WS_BYTES ((size_t)8 << 20)
+
+PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cache,
+                                       const uint16_t* v_cache, pkv_cache_desc cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, float scale,
+                                       const pkv_decode_plan* plan, uint16_t* out,
+                                       void* stream);
+
+/*
  * Varlen causal paged prefill [P1 PagedAttention; P3 prefix-cache hits share blocks].
  * Sequence b has q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens (rows cu_seqlens_q[b] ..
  * of q, k, v) and k_len = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys. The first P = k_len - q_len

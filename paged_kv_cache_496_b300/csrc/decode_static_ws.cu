@@ -1,0 +1,64 @@
+// decode_static_ws.cu -- paged decode for callers that cannot allocate device memory.
+//
+// pkv_paged_decode needs a device workspace (work list, claim counter, chunk partials) that the
+// caller allocates. Some callers cannot do that: a host process that has handed all of a GPU's
+// memory to its own pool allocator (so a cudaMalloc would fail or fragment that pool), or code
+// that must not enter an allocator at the point where it runs attention, such as a plugin called
+// from inside another runtime's execution loop. pkv_paged_decode_static_ws serves them: it runs
+// the same decode with the workspace placed in a fixed-size array in the library's own device
+// memory, PKV_STATIC_WS_BYTES long (a file-scope __device__ array that every GPU which loads the
+// library holds until the process exits). It calls no allocating routine.
+//
+// Sharing: every call on a device uses the same array, which keeps what the previous call left
+// in it. The decode's one-CTA plan kernel resets everything that must start at zero (the claim
+// counter and the per-chunk merge counters) at the start of each call, so nothing has to be
+// cleared here. Two calls that overlap on the GPU (different streams, no ordering between them)
+// race on the array and corrupt each other's results: order them, for example on one stream.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_workspace[PKV_STATIC_WS_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_workspace_addr[kMaxDevices] = {};
+std::mutex g_workspace_mutex;
+
+// Device address of the current device's copy of the array. Host code cannot use the symbol
+// itself (it names a host-side stand-in), so the first call on each device looks the address up
+// with that device current and keeps it.
+cudaError_t static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_workspace_mutex);
+  if (g_workspace_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    g_workspace_addr[dev] = p;
+  }
+  *out = g_workspace_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" PKV_API int pkv_paged_decode_static_ws(
+    const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, pkv_cache_desc cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t num_seqs, int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+    uint16_t* out, void* stream) {
+  void* ws = nullptr;
+  if (static_workspace(&ws) != cudaSuccess) return PKV_ERR_CUDA;
+  // pkv_paged_decode validates every argument and rejects a plan whose workspace exceeds
+  // PKV_STATIC_WS_BYTES (PKV_ERR_WORKSPACE_TOO_SMALL, with both sizes in pkv_last_error())
+  // before anything is enqueued.
+  return pkv_paged_decode(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          context_lens, num_seqs, num_q_heads, scale, plan, out, ws,
+                          (size_t)PKV_STATIC_WS_BYTES, stream);
+}
