@@ -81,13 +81,18 @@ struct Traits {
   static constexpr int kCbFloats = (GH * D + 2 * GH + 3) / 4 * 4;
   // Two CTAs per SM: keep each CTA within 112 KB of shared memory.
   static constexpr int kSmemBudget = 112 * 1024;
-  static constexpr int kFixedBytes = 2 * kWarps * kCbFloats * 4 + 8 * 32 + 160;
+  static constexpr int kFixedBytes =
+      2 * kWarps * kCbFloats * 4 + kWarps * kChunks * 4 * 8 * GH * 8 + 8 * 32 + 160;
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / (kStageBytes + kQBytes);
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kMaxSub = kTileT / 16;        // TMA boxes per tile at block_size 16
+  // Per-warp copy of the item's q, pre-scaled fp32 pairs: for (chunk c, word w) the 8 lanes of a
+  // group read consecutive 16-byte slots (two heads' pairs each), conflict-free.
+  static constexpr int kQfBytesPerWarp = kChunks * 4 * 8 * GH * 8;
   static constexpr int kOffTiles = 0;
   static constexpr int kOffQ = kOffTiles + kStages * kStageBytes;
-  static constexpr int kOffCb = kOffQ + kStages * kQBytes;
+  static constexpr int kOffQf = kOffQ + kStages * kQBytes;
+  static constexpr int kOffCb = kOffQf + kWarps * kQfBytesPerWarp;
   static constexpr int kOffMeta = kOffCb + 2 * kWarps * kCbFloats * 4;
   static constexpr int kOffBar = (kOffMeta + kStages * (int)sizeof(StageMeta) + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
@@ -255,7 +260,7 @@ __device__ __forceinline__ float sum_over_tokens(float x) {
 // ---------------------------------------------------------------------------------------------
 
 template <int D, int GH>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(168)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using T = Traits<D, GH>;
@@ -426,7 +431,7 @@ __global__ void __maxnreg__(200)
   const int my_t = j / GH;
   const int tbase = warp * T::kTokPerWarp + g * T::kTPG;
 
-  uint64_t qp[GH][T::kPairs];
+  uint8_t* qfw = smem + T::kOffQf + warp * T::kQfBytesPerWarp;  // this warp's q copy
   uint64_t acc[GH][T::kPairs];
   float m_ref[GH];
   float l_lane = 0.f;
@@ -439,10 +444,10 @@ __global__ void __maxnreg__(200)
       if (lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
       return;
     }
-    const StageMeta mt = meta[st];
-    if (mt.flags & kMetaDone) break;
+    const int mflags = meta[st].flags;
+    if (mflags & kMetaDone) break;
 
-    if (mt.flags & (kMetaFirst | kMetaZero)) {
+    if (mflags & (kMetaFirst | kMetaZero)) {
 #pragma unroll
       for (int h = 0; h < GH; ++h) {
         m_ref[h] = -INFINITY;
@@ -451,53 +456,89 @@ __global__ void __maxnreg__(200)
       }
       l_lane = 0.f;
     }
-    if (mt.flags & kMetaFirst) {
-      const uint8_t* qs = qbuf + st * T::kQBytes;
-      const uint64_t sc2 = pack2(p.qk_scale_log2, p.qk_scale_log2);
-#pragma unroll
-      for (int h = 0; h < GH; ++h)
-#pragma unroll
-        for (int c = 0; c < T::kChunks; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(qs + (h * D + (j + 8 * c) * 8) * 2);
-          qp[h][4 * c + 0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
-          qp[h][4 * c + 1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
-          qp[h][4 * c + 2] = fmul2(bf16x2_to_f32x2(w.z), sc2);
-          qp[h][4 * c + 3] = fmul2(bf16x2_to_f32x2(w.w), sc2);
-        }
-    }
-
-    if (!(mt.flags & kMetaZero)) {
-      const uint8_t* kt = tiles + st * T::kStageBytes;
-      const uint8_t* vt = kt + T::kTileBytes;
-      const int n_valid = mt.tok_end - mt.tok0;  // tokens of this tile that count (may exceed)
-
-      // ---- scores: partial q.k over this lane's dims for its TPG tokens x GH heads ----
-      float part[8];
-#pragma unroll
-      for (int tt = 0; tt < T::kTPG; ++tt) {
-        const uint8_t* row = kt + (tbase + tt) * T::kRowBytes;
-        uint64_t s2[GH];
-#pragma unroll
-        for (int h = 0; h < GH; ++h) s2[h] = 0ull;
+    if (mflags & kMetaFirst) {
+      // q of this item, scaled by scale*log2(e), into this warp's copy (lanes of group 0 write)
+      if (lane < 8) {
+        const uint8_t* qs = qbuf + st * T::kQBytes;
+        const uint64_t sc2 = pack2(p.qk_scale_log2, p.qk_scale_log2);
 #pragma unroll
         for (int c = 0; c < T::kChunks; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(row + (j + 8 * c) * 16);
-          const uint64_t k0 = bf16x2_to_f32x2(w.x), k1 = bf16x2_to_f32x2(w.y);
-          const uint64_t k2 = bf16x2_to_f32x2(w.z), k3 = bf16x2_to_f32x2(w.w);
+          uint64_t qv[GH][4];
 #pragma unroll
           for (int h = 0; h < GH; ++h) {
-            s2[h] = ffma2(qp[h][4 * c + 0], k0, s2[h]);
-            s2[h] = ffma2(qp[h][4 * c + 1], k1, s2[h]);
-            s2[h] = ffma2(qp[h][4 * c + 2], k2, s2[h]);
-            s2[h] = ffma2(qp[h][4 * c + 3], k3, s2[h]);
+            const uint4 w = *reinterpret_cast<const uint4*>(qs + (h * D + (j + 8 * c) * 8) * 2);
+            qv[h][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
+            qv[h][1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
+            qv[h][2] = fmul2(bf16x2_to_f32x2(w.z), sc2);
+            qv[h][3] = fmul2(bf16x2_to_f32x2(w.w), sc2);
+          }
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint8_t* base = qfw + (c * 4 + w) * (64 * GH);
+            if constexpr (GH == 1) {
+              *reinterpret_cast<uint64_t*>(base + j * 8) = qv[0][w];
+            } else {
+#pragma unroll
+              for (int hh = 0; hh < GH / 2; ++hh)
+                *reinterpret_cast<ulonglong2*>(base + hh * 128 + j * 16) =
+                    make_ulonglong2(qv[2 * hh][w], qv[2 * hh + 1][w]);
+            }
           }
         }
+      }
+      __syncwarp();
+    }
+
+    if (!(mflags & kMetaZero)) {
+      const uint8_t* kt = tiles + st * T::kStageBytes;
+      const uint8_t* vt = kt + T::kTileBytes;
+      const int n_valid = meta[st].tok_end - meta[st].tok0;  // tokens that count (may exceed)
+
+      // ---- scores: partial q.k over this lane's dims for its TPG tokens x GH heads ----
+      uint64_t s2[T::kTPG][GH];
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-          const float2 f = unpack2(s2[h]);
-          part[tt * GH + h] = f.x + f.y;
+      for (int tt = 0; tt < T::kTPG; ++tt)
+#pragma unroll
+        for (int h = 0; h < GH; ++h) s2[tt][h] = 0ull;
+#pragma unroll
+      for (int c = 0; c < T::kChunks; ++c) {
+        uint4 kw[T::kTPG];
+#pragma unroll
+        for (int tt = 0; tt < T::kTPG; ++tt)
+          kw[tt] = *reinterpret_cast<const uint4*>(kt + (tbase + tt) * T::kRowBytes +
+                                                   (j + 8 * c) * 16);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint64_t qv[GH];
+          const uint8_t* base = qfw + (c * 4 + w) * (64 * GH);
+          if constexpr (GH == 1) {
+            qv[0] = *reinterpret_cast<const uint64_t*>(base + j * 8);
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < GH / 2; ++hh) {
+              const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(base + hh * 128 + j * 16);
+              qv[2 * hh] = v.x;
+              qv[2 * hh + 1] = v.y;
+            }
+          }
+#pragma unroll
+          for (int tt = 0; tt < T::kTPG; ++tt) {
+            const uint32_t word = w == 0 ? kw[tt].x : w == 1 ? kw[tt].y : w == 2 ? kw[tt].z
+                                                                                   : kw[tt].w;
+            const uint64_t kp = bf16x2_to_f32x2(word);
+#pragma unroll
+            for (int h = 0; h < GH; ++h) s2[tt][h] = ffma2(qv[h], kp, s2[tt][h]);
+          }
         }
       }
+      float part[8];
+#pragma unroll
+      for (int tt = 0; tt < T::kTPG; ++tt)
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          const float2 f = unpack2(s2[tt][h]);
+          part[tt * GH + h] = f.x + f.y;
+        }
       float sc = reduce_scatter8(part, j);
       const bool valid = (tbase + my_t) < n_valid;
       sc = valid ? sc : -INFINITY;
@@ -557,11 +598,21 @@ __global__ void __maxnreg__(200)
         }
       }
     }
+    if (!(mflags & (kMetaLast | kMetaZero))) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      ++use;
+      continue;
+    }
+    // Last tile of the item: take its identity from the stage before releasing the stage.
+    StageMeta mt;
+    mt.b = meta[st].b;
+    mt.x = meta[st].x;
+    mt.split = meta[st].split;
+    mt.nsplit = meta[st].nsplit;
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
     ++use;
-
-    if (!(mt.flags & (kMetaLast | kMetaZero))) continue;
 
     // ---- item finished: merge the lane groups, then the warps, then write ----
 #pragma unroll
@@ -686,6 +737,11 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
     cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, GH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // the largest shared-memory carve-out, so that two CTAs fit on an SM
+    e = cudaFuncSetAttribute(paged_decode_kernel<D, GH>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, GH>,
