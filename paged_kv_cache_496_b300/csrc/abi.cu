@@ -265,10 +265,8 @@ int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
   DeviceInfo d;
   st = device_info(&d);
   if (st != PKV_OK) return st;
-  const int G = num_q_heads / cache.num_kv_heads;
-  const int GH = G >= 4 ? 4 : G;
-  const int tile = 128 / GH;
-  const int box_t = cache.block_size < tile ? cache.block_size : tile;
+  const int box_t = decode_box_rows(cache.head_dim, num_q_heads / cache.num_kv_heads,
+                                    cache.block_size);
   CUtensorMap tk, tv;
   const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
   st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,

@@ -48,6 +48,9 @@ struct DecodeArgs {
   int* flags;
 };
 
+// Rows of the K/V TMA box the decode kernel expects (tile tokens, or the block size if smaller).
+int decode_box_rows(int head_dim, int group, int block_size);
+
 // Returns a CUDA error, or cudaErrorNotSupported for shapes without an instance.
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                 const CUtensorMap& tmap_v, int num_sms, cudaStream_t stream);

@@ -68,9 +68,14 @@ template <int D, int GH>
 struct Traits {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kTPG = 8 / GH;                  // tokens per lane group per tile
+  // Each lane starts with kN partial scores, one per (token, head) pair of its lane group, and
+  // ends the reduce-scatter holding kVPL full scores. Four-head groups take 16 pairs (4 tokens),
+  // which doubles the independent work per softmax step; smaller groups take 8.
+  static constexpr int kN = GH == 4 ? 16 : 8;
+  static constexpr int kVPL = kN / 8;
+  static constexpr int kTPG = kN / GH;                 // tokens per lane group per tile
   static constexpr int kTokPerWarp = 4 * kTPG;
-  static constexpr int kTileT = kWarps * kTokPerWarp;  // 128 / GH tokens per tile
+  static constexpr int kTileT = kWarps * kTokPerWarp;  // tokens per tile (64 or 128)
   static constexpr int kChunks = D / 64;               // 16-byte chunks per lane per row
   static constexpr int kPairs = D / 16;                // fp32 pairs per lane per row
   static constexpr int kRowBytes = D * 2;
@@ -96,7 +101,7 @@ struct Traits {
   static constexpr int kOffMeta = kOffCb + 2 * kWarps * kCbFloats * 4;
   static constexpr int kOffBar = (kOffMeta + kStages * (int)sizeof(StageMeta) + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
-  static_assert(kTPG * GH == 8, "one (token, head) score per lane of a group");
+  static_assert(kTPG * GH == kN && (kN == 8 || kN == 16), "lane-group pair layout");
   static_assert(kCbFloats % 4 == 0, "float4 stores into the combine slots");
   static_assert(kQBytes % 16 == 0 && kOffQ % 128 == 0 && kOffCb % 16 == 0, "smem alignment");
   static_assert(kOffMeta % 16 == 0 && kOffBar % 16 == 0, "smem alignment");
@@ -210,48 +215,42 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
 // Register-level pieces of the consumer
 // ---------------------------------------------------------------------------------------------
 
-// Eight partial sums per lane, one per (token, head) pair of the lane group, summed over the
-// group's eight lanes; afterwards lane j of the group holds the full sum of pair j.
-__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int j) {
-  {
-    const bool up = j & 4;
+// N partial sums per lane, one per (token, head) pair idx = token * GH + head of the lane group,
+// summed over the group's eight lanes by three halving exchanges (lane masks 4, 2, 1). Afterwards
+// lane j holds the full sums of pairs j*N/8 .. j*N/8 + N/8 - 1 in v[0 .. N/8 - 1].
+template <int N>
+__device__ __forceinline__ void reduce_scatter(float (&v)[N], int j) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = up ? v[i] : v[i + 4];
-      const float keep = up ? v[i + 4] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFullMask, send, 4);
+  for (int step = 0; step < 3; ++step) {
+    const int m = 4 >> step;
+    const int half = N >> (step + 1);
+    const bool up = j & m;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, m);
     }
   }
-  {
-    const bool up = j & 2;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float send = up ? v[i] : v[i + 2];
-      const float keep = up ? v[i + 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFullMask, send, 2);
-    }
-  }
-  {
-    const bool up = j & 1;
-    const float send = up ? v[0] : v[1];
-    const float keep = up ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(kFullMask, send, 1);
-  }
-  return v[0];
 }
 
-// Lanes holding the same head differ only in the bits >= GH (token within the group, group).
-template <int GH>
+// After the reduce-scatter, lane bit b (< 3) moves a held pair index by 2^b * N/8 and the group
+// bits (3, 4) select other tokens. A lane bit that moves the index by a multiple of GH keeps the
+// head and changes only the token, so reducing over those bits combines one head's tokens.
+template <int N, int GH>
 __device__ __forceinline__ float max_over_tokens(float x) {
 #pragma unroll
-  for (int m = GH; m < 32; m <<= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, m));
+  for (int b = 0; b < 5; ++b)
+    if (b >= 3 || ((1 << b) * (N / 8)) % GH == 0)
+      x = fmaxf(x, __shfl_xor_sync(kFullMask, x, 1 << b));
   return x;
 }
 
-template <int GH>
+template <int N, int GH>
 __device__ __forceinline__ float sum_over_tokens(float x) {
 #pragma unroll
-  for (int m = GH; m < 32; m <<= 1) x += __shfl_xor_sync(kFullMask, x, m);
+  for (int b = 0; b < 5; ++b)
+    if (b >= 3 || ((1 << b) * (N / 8)) % GH == 0) x += __shfl_xor_sync(kFullMask, x, 1 << b);
   return x;
 }
 
@@ -425,16 +424,20 @@ __global__ void __maxnreg__(168)
   }
 
   // ================================= consumer warps =================================
+  constexpr int VPL = T::kVPL;
   const int g = lane >> 3;  // lane group: tokens [g*TPG, (g+1)*TPG) of this warp's share
   const int j = lane & 7;   // dims [(j + 8c) * 8, +8) for chunk c
-  const int my_h = j % GH;  // after the reduce-scatter this lane holds pair (j / GH, j % GH)
-  const int my_t = j / GH;
+  // after the reduce-scatter this lane holds pairs idx = j*VPL + r: token idx/GH, head idx%GH
+  auto my_h = [j](int r) { return (j * VPL + r) % GH; };
+  auto my_t = [j](int r) { return (j * VPL + r) / GH; };
   const int tbase = warp * T::kTokPerWarp + g * T::kTPG;
 
   uint8_t* qfw = smem + T::kOffQf + warp * T::kQfBytesPerWarp;  // this warp's q copy
   uint64_t acc[GH][T::kPairs];
   float m_ref[GH];
-  float l_lane = 0.f;
+  float l_lane[VPL];
+#pragma unroll
+  for (int r = 0; r < VPL; ++r) l_lane[r] = 0.f;
   uint32_t use = 0;
   uint32_t item = 0;
 
@@ -454,7 +457,8 @@ __global__ void __maxnreg__(168)
 #pragma unroll
         for (int i = 0; i < T::kPairs; ++i) acc[h][i] = 0ull;
       }
-      l_lane = 0.f;
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) l_lane[r] = 0.f;
     }
     if (mflags & kMetaFirst) {
       // q of this item, scaled by scale*log2(e), into this warp's copy (lanes of group 0 write)
@@ -531,7 +535,7 @@ __global__ void __maxnreg__(168)
           }
         }
       }
-      float part[8];
+      float part[T::kN];
 #pragma unroll
       for (int tt = 0; tt < T::kTPG; ++tt)
 #pragma unroll
@@ -539,15 +543,20 @@ __global__ void __maxnreg__(168)
           const float2 f = unpack2(s2[tt][h]);
           part[tt * GH + h] = f.x + f.y;
         }
-      float sc = reduce_scatter8(part, j);
-      const bool valid = (tbase + my_t) < n_valid;
-      sc = valid ? sc : -INFINITY;
+      reduce_scatter<T::kN>(part, j);
+      float sc[VPL], mx[VPL];
+      bool valid[VPL];
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        valid[r] = (tbase + my_t(r)) < n_valid;
+        sc[r] = valid[r] ? part[r] : -INFINITY;
+        mx[r] = max_over_tokens<T::kN, GH>(sc[r]);
+      }
 
       // ---- online softmax (log2 units), lazy rescale ----
-      const float mx = max_over_tokens<GH>(sc);
-      float mt_all[GH];
+      float mt_all[GH];  // head h sits in lane h / VPL of group 0, slot h % VPL
 #pragma unroll
-      for (int h = 0; h < GH; ++h) mt_all[h] = __shfl_sync(kFullMask, mx, h);
+      for (int h = 0; h < GH; ++h) mt_all[h] = __shfl_sync(kFullMask, mx[h % VPL], h / VPL);
       bool need = false;
 #pragma unroll
       for (int h = 0; h < GH; ++h) need |= mt_all[h] > m_ref[h] + kTau;
@@ -559,17 +568,23 @@ __global__ void __maxnreg__(168)
             const uint64_t a2 = pack2(alpha, alpha);
 #pragma unroll
             for (int i = 0; i < T::kPairs; ++i) acc[h][i] = fmul2(acc[h][i], a2);
-            if (my_h == h) l_lane *= alpha;
+#pragma unroll
+            for (int r = 0; r < VPL; ++r)
+              if (my_h(r) == h) l_lane[r] *= alpha;
             m_ref[h] = mt_all[h];
           }
         }
       }
-      float my_m = m_ref[0];
+      float pr[VPL];
 #pragma unroll
-      for (int h = 1; h < GH; ++h)
-        if (my_h == h) my_m = m_ref[h];
-      const float pr = valid ? fast_exp2(sc - my_m) : 0.f;
-      l_lane += pr;
+      for (int r = 0; r < VPL; ++r) {
+        float my_m = m_ref[0];
+#pragma unroll
+        for (int h = 1; h < GH; ++h)
+          if (my_h(r) == h) my_m = m_ref[h];
+        pr[r] = valid[r] ? fast_exp2(sc[r] - my_m) : 0.f;
+        l_lane[r] += pr[r];
+      }
 
       // ---- acc += p * V over this lane group's tokens ----
 #pragma unroll
@@ -577,17 +592,18 @@ __global__ void __maxnreg__(168)
         uint64_t pp[GH];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
-          const float pv = __shfl_sync(kFullMask, pr, (lane & ~7) | (tt * GH + h));
+          const int idx = tt * GH + h;  // held by lane idx / VPL of this group, slot idx % VPL
+          const float pv = __shfl_sync(kFullMask, pr[idx % VPL], (lane & ~7) | (idx / VPL));
           pp[h] = pack2(pv, pv);
         }
-        const bool tok_ok = (tbase + tt) < n_valid;
+        // stale shared memory past the end of the context must not reach the products
+        const uint32_t keep = (tbase + tt) < n_valid ? 0xffffffffu : 0u;
         const uint8_t* row = vt + (tbase + tt) * T::kRowBytes;
 #pragma unroll
         for (int c = 0; c < T::kChunks; ++c) {
-          uint4 w = *reinterpret_cast<const uint4*>(row + (j + 8 * c) * 16);
-          if (!tok_ok) w = make_uint4(0u, 0u, 0u, 0u);  // stale shared memory past the end
-          const uint64_t v0 = bf16x2_to_f32x2(w.x), v1 = bf16x2_to_f32x2(w.y);
-          const uint64_t v2 = bf16x2_to_f32x2(w.z), v3 = bf16x2_to_f32x2(w.w);
+          const uint4 w = *reinterpret_cast<const uint4*>(row + (j + 8 * c) * 16);
+          const uint64_t v0 = bf16x2_to_f32x2(w.x & keep), v1 = bf16x2_to_f32x2(w.y & keep);
+          const uint64_t v2 = bf16x2_to_f32x2(w.z & keep), v3 = bf16x2_to_f32x2(w.w & keep);
 #pragma unroll
           for (int h = 0; h < GH; ++h) {
             acc[h][4 * c + 0] = ffma2(pp[h], v0, acc[h][4 * c + 0]);
@@ -626,7 +642,12 @@ __global__ void __maxnreg__(168)
         v.y += __shfl_xor_sync(kFullMask, v.y, 16);
         acc[h][i] = pack2(v.x, v.y);
       }
-    const float l_warp = sum_over_tokens<GH>(l_lane);  // lane h now holds head h's sum
+    float l_sum[VPL];
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) l_sum[r] = sum_over_tokens<T::kN, GH>(l_lane[r]);
+    float l_all[GH];
+#pragma unroll
+    for (int h = 0; h < GH; ++h) l_all[h] = __shfl_sync(kFullMask, l_sum[h % VPL], h / VPL);
     const int par = item & 1;
     float* cbw = cb + (par * T::kWarps + warp) * T::kCbFloats;
     if (g == 0) {
@@ -641,13 +662,12 @@ __global__ void __maxnreg__(168)
           reinterpret_cast<float4*>(dst)[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
         }
     }
-    if (lane < GH) {
-      float mm = m_ref[0];
+    if (lane == 0) {
 #pragma unroll
-      for (int h = 1; h < GH; ++h)
-        if (lane == h) mm = m_ref[h];
-      cbw[GH * D + lane] = mm;
-      cbw[GH * D + GH + lane] = l_warp;
+      for (int h = 0; h < GH; ++h) {
+        cbw[GH * D + h] = m_ref[h];
+        cbw[GH * D + GH + h] = l_all[h];
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(cmb0 + 8 * par);
@@ -831,6 +851,19 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t hea
     carve->part_ml = max_splits > 1 ? reinterpret_cast<float2*>(b8 + ml) : nullptr;
   }
   return off;
+}
+
+int decode_box_rows(int head_dim, int group, int block_size) {
+  const int GH = group >= 4 ? 4 : group;
+  int tile = 0;
+  if (head_dim == 128) {
+    tile = GH == 4 ? Traits<128, 4>::kTileT : GH == 2 ? Traits<128, 2>::kTileT
+                                                     : Traits<128, 1>::kTileT;
+  } else {
+    tile = GH == 4 ? Traits<64, 4>::kTileT : GH == 2 ? Traits<64, 2>::kTileT
+                                                    : Traits<64, 1>::kTileT;
+  }
+  return block_size < tile ? block_size : tile;
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
