@@ -68,7 +68,7 @@ def profiled_traffic(kernel_key, source):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -81,7 +81,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                   "-lms", "200"]
+                   "-lms", "50"]
             if self.gpu_id:
                 cmd += ["-i", self.gpu_id]
             self.f = open(self.path, "w")
@@ -131,11 +131,13 @@ class ClockSampler:
 class DecodeStep:
     """All layers of one decode step, resident in HBM."""
 
-    def __init__(self, name, torch, pk, device, log_fill=True):
+    def __init__(self, name, torch, pk, device, log_fill=True, num_seqs=None, num_layers=None):
         self.w = w = W.WORKLOADS[name]
         self.torch, self.pk = torch, pk
         self.ctx = W.decode_lengths(name)
-        self.B, self.L = len(self.ctx), w.num_layers
+        if num_seqs:
+            self.ctx = self.ctx[:num_seqs]
+        self.B, self.L = len(self.ctx), (num_layers or w.num_layers)
         self.bt, self.nb = W.place_blocks(W.rng_for(w.seed, 10, 0), self.ctx, w.block_size)
         self.slots = W.slots_for_positions(self.bt, np.arange(self.B), self.ctx - 1, w.block_size)
         pool_shape = (self.nb, w.block_size, w.num_kv_heads, w.head_dim)
@@ -264,12 +266,17 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_decode")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: fewer layers than the workload (not a bench number)")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="profiling only: the first N sequences (not a bench number)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -291,7 +298,9 @@ def main():
     if gpu_uuid and not gpu_uuid.startswith("GPU-"):
         gpu_uuid = "GPU-" + gpu_uuid
 
-    step = DecodeStep(args.workload, torch, pk, device)
+    step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
+                      num_layers=args.layers)
+    reduced = bool(args.num_seqs or args.layers)
     w = step.w
 
     def barrier():
@@ -340,7 +349,7 @@ def main():
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
-    if True:
+    if not args.no_e2e:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         h_q = [pin(x) for x in step.q]
         h_k = [pin(x) for x in step.k_new]
@@ -385,7 +394,7 @@ def main():
         extras = secondary_measurements(torch, pk, device, step)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not reduced:
         r = time_oracle(args.workload)
         cpu = {"value": r["gbs"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['n_seqs']} sequences x 1 layer (store + decode), "
@@ -407,7 +416,8 @@ def main():
                        "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
                        "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
                        "step": "per layer: kv_store (1 token/seq) + paged_decode",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       "reduced_for_profiling": reduced},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "paged_decode (plan + persistent decode kernel)",

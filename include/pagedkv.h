@@ -60,6 +60,7 @@ extern "C" {
 #define PKV_DEVERR_CTX_CLAMPED 4    /* a context longer than its block table or the decode plan */
 #define PKV_DEVERR_TIMEOUT 8        /* an internal pipeline wait gave up after one second */
 #define PKV_DEVERR_BAD_LENGTHS 16   /* prefill: cu_seqlens not increasing or k_len < q_len */
+#define PKV_DEVERR_INTERNAL 32      /* an internal layout invariant failed (nothing written) */
 
 /* Geometry of one layer's paged cache. */
 typedef struct pkv_cache_desc {
@@ -180,6 +181,8 @@ PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cach
  *       NULL: there is no prefix (cu_seqlens_k must equal cu_seqlens_q) and keys are read from
  *       k and v directly; k_cache and v_cache may then be NULL.
  *   out           device, [total_q, num_q_heads, head_dim] bf16
+ * Runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory); supports
+ * head_dim 128 and group sizes 1, 2, 4, 8 (other shapes return PKV_ERR_UNSUPPORTED).
  */
 PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,

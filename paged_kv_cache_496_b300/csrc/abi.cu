@@ -87,15 +87,16 @@ int get_encoder(EncodeTiledFn* fn) {
   return PKV_OK;
 }
 
-// 3-D view {D, heads, rows} of a row-major [rows, heads, D] bf16 tensor; box {box_d, 1, box_rows}.
+// 3-D view {D, heads, rows} of a row-major [rows, heads, D] bf16 tensor;
+// box {box_d, box_heads, box_rows}.
 int encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int head_dim,
-                    int box_d, int box_rows, CUtensorMapSwizzle swizzle) {
+                    int box_d, int box_rows, CUtensorMapSwizzle swizzle, int box_heads = 1) {
   EncodeTiledFn enc;
   int st = get_encoder(&enc);
   if (st != PKV_OK) return st;
   const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows};
+  const cuuint32_t box[3] = {(cuuint32_t)box_d, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
@@ -303,11 +304,76 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       const uint16_t* v_cache, pkv_cache_desc cache, int32_t num_q_heads,
                       float scale, uint16_t* out, void* stream) {
   g_last_error[0] = 0;
-  (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)num_seqs;
-  (void)total_q; (void)max_seqlen_q; (void)block_tables; (void)max_blocks_per_seq;
-  (void)k_cache; (void)v_cache; (void)cache; (void)num_q_heads; (void)scale; (void)out;
-  (void)stream;
-  return fail(PKV_ERR_UNSUPPORTED, "paged_prefill is not built yet");
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs, total_q and max_seqlen_q must be >= 0");
+  if (cache.num_kv_heads <= 0 || cache.head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads and head_dim must be positive");
+  if (cache.head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_prefill supports head_dim 128 (got %d)",
+                cache.head_dim);
+  int st = check_heads(num_q_heads, cache.num_kv_heads);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(PKV_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  const bool paged = block_tables != nullptr;
+  if (paged) {
+    st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (!k_cache || !v_cache) return fail(PKV_ERR_INVALID_ARG, "null cache pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+      return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+    if (max_blocks_per_seq <= 0)
+      return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
+  }
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+    return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  DeviceInfo d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  const int G = num_q_heads / cache.num_kv_heads;
+  CUtensorMap tq, tk, tv;
+  st = encode_rows_map(&tq, q, total_q, num_q_heads, 128, 64, prefill_positions_per_tile(G),
+                       CU_TENSOR_MAP_SWIZZLE_128B, G);
+  if (st != PKV_OK) return st;
+  const int box = prefill_kv_box_rows(cache.block_size, paged);
+  if (paged) {
+    const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
+    st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, 128, 64, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == PKV_OK)
+      st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, 128, 64, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    st = encode_rows_map(&tk, k, total_q, cache.num_kv_heads, 128, 64, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == PKV_OK)
+      st = encode_rows_map(&tv, v, total_q, cache.num_kv_heads, 128, 64, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (st != PKV_OK) return st;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_seqlen_q = max_seqlen_q;
+  a.block_tables = block_tables;
+  a.max_blocks = paged ? max_blocks_per_seq : 0;
+  a.cache = cache;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.out = out;
+  a.flags = d.flags;
+  cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d.num_sms,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
+  return PKV_OK;
 }
 
 }  // extern "C"

@@ -73,6 +73,10 @@ struct PrefillArgs {
   int* flags;
 };
 
+// Query positions per 128-row prefill tile, and rows per K/V TMA box.
+int prefill_positions_per_tile(int group);
+int prefill_kv_box_rows(int block_size, bool paged);
+
 cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tmap_q,
                                  const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                  int num_sms, cudaStream_t stream);

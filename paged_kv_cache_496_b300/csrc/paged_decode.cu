@@ -127,7 +127,7 @@ struct PlanParams {
   int32_t fixed_split;   // > 0: use exactly this chunk length
   int32_t head_groups;
   int32_t slots;         // resident CTAs of the decode grid
-  int32_t num_counters;  // entries of `counters` to zero (0 when nothing is split)
+  int32_t counters_per_seq;  // merge counters per sequence (0 when nothing can be split)
 };
 
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
   const int per = (pp.num_seqs + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(pp.num_seqs, tid * per);
   const int b1 = min(pp.num_seqs, b0 + per);
-  for (int i = tid; i < pp.num_counters; i += kPlanThreads) pp.counters[i] = 0u;
   // total tokens (for the chunk length) -- in units of 16 tokens to stay within 32 bits
   uint32_t local_tok = 0;
   for (int b = b0; b < b1; ++b) {
@@ -204,6 +203,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
     const int ctx = min(pp.context_lens[b], pp.cap_tokens);
     const int n = ctx > 0 ? (ctx + S - 1) / S : 1;
     for (int s = 0; s < n; ++s) pp.items[pos++] = make_int2(b, s);
+    // only split sequences use merge counters
+    if (n > 1)
+      for (int i = 0; i < pp.counters_per_seq; ++i)
+        pp.counters[(int64_t)b * pp.counters_per_seq + i] = 0u;
   }
   if (tid == 0) {
     pp.header[1] = total;  // number of (sequence, chunk) items
@@ -813,7 +816,7 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   pp.fixed_split = a.auto_split ? 0 : a.split_tokens;
   pp.head_groups = p.head_groups;
   pp.slots = (int32_t)((int64_t)num_sms * ctas_per_sm);
-  pp.num_counters = a.max_splits > 1 ? a.num_seqs * p.head_groups * T::kWarps : 0;
+  pp.counters_per_seq = a.max_splits > 1 ? p.head_groups * T::kWarps : 0;
   decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

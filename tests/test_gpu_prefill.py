@@ -1,0 +1,153 @@
+"""GPU parity: varlen causal paged prefill (tcgen05) through the C ABI against the fp64 oracle.
+
+The new tokens are stored with kv_store first (as the engine does); the kernel then reads every key
+through the block table. The oracle reads the cached prefix through the table and the new keys from
+k/v directly, so the two share no step. Bar: max-abs error <= 2e-2 on N(0,1) inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_496_b300 as pk
+import workloads as W
+from tests.gpu_util import TOL, assert_attn_close, dev_bf16, dev_i32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pk.get_device_error()
+    yield
+    assert pk.get_device_error() == 0
+
+
+def _run_paged(case: W.PrefillCase):
+    kc, vc = dev_bf16(case.k_cache), dev_bf16(case.v_cache)
+    k, v = dev_bf16(case.k), dev_bf16(case.v)
+    if len(case.slot_mapping):
+        pk.kv_store(k, v, dev_i32(case.slot_mapping), kc, vc)
+    out = pk.paged_prefill(dev_bf16(case.q), k, v, dev_i32(case.cu_seqlens_q),
+                           dev_i32(case.cu_seqlens_k), dev_i32(case.block_tables), case.scale,
+                           k_cache=kc, v_cache=vc,
+                           max_seqlen_q=int(case.q_lens.max(initial=0)))
+    assert pk.get_device_error() == 0
+    return out, kc, vc
+
+
+def _oracle(orc, case):
+    return orc.paged_prefill(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
+                             case.block_tables, case.k_cache, case.v_cache, case.scale)
+
+
+def test_prefill_single_tile_no_prefix(orc):
+    """One sequence, one CTA tile, keys read from k/v directly (no block table)."""
+    rng = W.rng_for(61, 0)
+    Hq, Hkv, D = 32, 8, 128
+    ql = np.array([20], np.int32)
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(ql.sum())
+    q, k, v = (W.normal_bf16(rng, (T, Hq, D)), W.normal_bf16(rng, (T, Hkv, D)),
+               W.normal_bf16(rng, (T, Hkv, D)))
+    out = pk.paged_prefill(dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_i32(cu), dev_i32(cu), None,
+                           1 / np.sqrt(D), max_seqlen_q=int(ql.max()))
+    assert pk.get_device_error() == 0
+    empty = np.zeros((1, 16, Hkv, D), np.uint16)
+    ref = orc.paged_prefill(q, k, v, cu, cu, None, empty, empty, 1 / np.sqrt(D))
+    assert_attn_close(out, ref, what="single tile")
+
+
+@pytest.mark.parametrize("qlens", [[1, 37, 130], [64, 65, 200, 0, 3]], ids=["a", "b"])
+def test_prefill_no_prefix_varlen(orc, qlens):
+    rng = W.rng_for(62, len(qlens))
+    Hq, Hkv, D = 32, 8, 128
+    ql = np.array(qlens, np.int32)
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(ql.sum())
+    q, k, v = (W.normal_bf16(rng, (T, Hq, D)), W.normal_bf16(rng, (T, Hkv, D)),
+               W.normal_bf16(rng, (T, Hkv, D)))
+    out = pk.paged_prefill(dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_i32(cu), dev_i32(cu), None,
+                           1 / np.sqrt(D), max_seqlen_q=int(ql.max()))
+    assert pk.get_device_error() == 0
+    empty = np.zeros((1, 16, Hkv, D), np.uint16)
+    ref = orc.paged_prefill(q, k, v, cu, cu, None, empty, empty, 1 / np.sqrt(D))
+    assert_attn_close(out, ref, what=f"no prefix {qlens}")
+
+
+@pytest.mark.parametrize("BS", [256, 64, 16])
+@pytest.mark.parametrize("q_scale", [1.0, 8.0], ids=["normal", "sharp"])
+def test_prefill_shared_prefix(orc, BS, q_scale):
+    case = W.prefix_prefill_case(63, 4, 256, 1, 300, 32, 8, 128, BS, q_scale=q_scale,
+                                 suffix_lens=np.array([1, 63, 64, 300]))
+    out, _, _ = _run_paged(case)
+    assert_attn_close(out, _oracle(orc, case), what=f"prefix BS={BS} q_scale={q_scale}")
+
+
+@pytest.mark.parametrize("Hq", [8, 16, 64], ids=["G1", "G2", "G8"])
+def test_prefill_group_sizes(orc, Hq):
+    case = W.prefix_prefill_case(64, 3, 128, 1, 200, Hq, 8, 128, 64,
+                                 suffix_lens=np.array([5, 129, 200]))
+    out, _, _ = _run_paged(case)
+    assert_attn_close(out, _oracle(orc, case), what=f"Hq={Hq}")
+
+
+def test_prefill_row_equals_decode():
+    """Prefill query i equals decode over the first P + i + 1 keys of the same cache."""
+    case = W.prefix_prefill_case(65, 2, 256, 40, 90, 32, 8, 128, 256)
+    out, kc, vc = _run_paged(case)
+    for b in range(case.num_seqs):
+        P = int(case.k_lens[b] - case.q_lens[b])
+        rows = np.arange(case.cu_seqlens_q[b], case.cu_seqlens_q[b + 1])
+        ctx = P + 1 + np.arange(len(rows))
+        bt = np.repeat(case.block_tables[b:b + 1], len(rows), axis=0)
+        q = dev_bf16(case.q[rows])
+        d = pk.paged_decode(q, kc, vc, dev_i32(bt), dev_i32(ctx), case.scale,
+                            max_context_len=int(ctx.max()))
+        err = (d.float() - out[torch.as_tensor(rows, device="cuda")].float()).abs().max().item()
+        assert err <= TOL, err
+
+
+def test_prefill_bad_lengths_flagged():
+    case = W.prefix_prefill_case(66, 2, 256, 10, 20, 32, 8, 128, 256)
+    cu_k = case.cu_seqlens_k.copy()
+    cu_k[1] = cu_k[0] + int(case.q_lens[0]) - 1  # k_len < q_len for sequence 0
+    kc, vc = dev_bf16(case.k_cache), dev_bf16(case.v_cache)
+    k, v = dev_bf16(case.k), dev_bf16(case.v)
+    pk.get_device_error()
+    pk.paged_prefill(dev_bf16(case.q), k, v, dev_i32(case.cu_seqlens_q), dev_i32(cu_k),
+                     dev_i32(case.block_tables), case.scale, k_cache=kc, v_cache=vc)
+    assert pk.get_device_error() & pk.DEVERR_BAD_LENGTHS
+
+
+def test_prefill_bad_block_flagged_not_faulted():
+    case = W.prefix_prefill_case(67, 2, 256, 10, 20, 32, 8, 128, 256)
+    bt = case.block_tables.copy()
+    bt[0, 0] = case.num_blocks + 3
+    kc, vc = dev_bf16(case.k_cache), dev_bf16(case.v_cache)
+    pk.get_device_error()
+    pk.paged_prefill(dev_bf16(case.q), dev_bf16(case.k), dev_bf16(case.v),
+                     dev_i32(case.cu_seqlens_q), dev_i32(case.cu_seqlens_k), dev_i32(bt),
+                     case.scale, k_cache=kc, v_cache=vc)
+    assert pk.get_device_error() & pk.DEVERR_BAD_BLOCK
+
+
+@pytest.mark.slow
+def test_full_prefix_prefill_workload(orc):
+    """64 sequences sharing a 1024-token prefix (4 blocks of 256), U{100..1024} new tokens each,
+    in the launch configuration the benchmark times; sampled sequences against the oracle."""
+    ql = W.prefix_prefill_suffix_lengths()
+    case = W.prefix_prefill_case(4, 64, 1024, 100, 1024, 32, 8, 128, 256, suffix_lens=ql)
+    out, _, _ = _run_paged(case)
+    assert torch.isfinite(out.float()).all()
+    for b in (int(np.argmax(ql)), int(np.argmin(ql)), 17):
+        sub = W.PrefillCase(case.num_blocks, 256, 8, 128, 32, case.k_cache, case.v_cache,
+                            case.q[case.cu_seqlens_q[b]:case.cu_seqlens_q[b + 1]],
+                            case.k[case.cu_seqlens_q[b]:case.cu_seqlens_q[b + 1]],
+                            case.v[case.cu_seqlens_q[b]:case.cu_seqlens_q[b + 1]],
+                            np.array([0, ql[b]], np.int32),
+                            np.array([0, ql[b] + 1024], np.int32), case.block_tables[b:b + 1],
+                            case.slot_mapping[:0], case.scale)
+        ref = _oracle(orc, sub)
+        rows = slice(int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1]))
+        assert_attn_close(out[rows], ref, what=f"full workload seq {b}")
