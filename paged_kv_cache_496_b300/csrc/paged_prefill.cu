@@ -88,12 +88,13 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- which (sequence, kv head, query tile): largest query tiles (most keys) first ----
+  // ---- which (sequence, kv head, query tile): the query tiles of one (sequence, kv head) are
+  // adjacent, longest first, so they run together and share that head's K/V through L2 ----
   const int id = blockIdx.x;
-  const int g = id % p.num_kv_heads;
-  const int t = id / p.num_kv_heads;
-  const int b = t % p.num_seqs;
-  const int qt = p.num_q_tiles - 1 - t / p.num_seqs;
+  const int qt = p.num_q_tiles - 1 - id % p.num_q_tiles;
+  const int t = id / p.num_q_tiles;
+  const int g = t % p.num_kv_heads;
+  const int b = t / p.num_kv_heads;
   const int q_start = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - q_start;
   const int k_len = p.cu_k[b + 1] - p.cu_k[b];
@@ -300,18 +301,31 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       if (lane == 0) mbar_arrive(bar(kBarSFree));
 
       const int kbase = j * kKeys;
+      // Tiles below every row's causal limit and inside k_len need no mask (CTA-uniform test);
+      // there, with a positive scale, max and exp take the raw scores: p = 2^(s*c - m).
+      const bool full = kbase + kKeys - 1 <= P + q0 && kbase + kKeys <= k_len &&
+                        p.qk_scale_log2 > 0.f;
       float mt = -INFINITY;
+      if (full) {
+        float mraw = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int key = kbase + h * 32 + c;
-          const float s = (key <= limit && key < k_len)
-                              ? __uint_as_float(sr[h][c]) * p.qk_scale_log2
-                              : -INFINITY;
-          sr[h][c] = __float_as_uint(s);
-          mt = fmaxf(mt, s);
-        }
+          for (int c = 0; c < 32; ++c) mraw = fmaxf(mraw, __uint_as_float(sr[h][c]));
+        mt = mraw * p.qk_scale_log2;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int key = kbase + h * 32 + c;
+            const float s = (key <= limit && key < k_len)
+                                ? __uint_as_float(sr[h][c]) * p.qk_scale_log2
+                                : -INFINITY;
+            sr[h][c] = __float_as_uint(s);
+            mt = fmaxf(mt, s);
+          }
+      }
       const bool resc = mt > m_run + kTauP;
       float alpha = 1.f;
       if (resc) {
@@ -320,16 +334,29 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       }
       float sum = 0.f;
       uint32_t pk[32];
+      if (full) {
+        const float c2 = p.qk_scale_log2, nm = -m_run;
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float s0 = __uint_as_float(sr[h][c]), s1 = __uint_as_float(sr[h][c + 1]);
-          const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
-          const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
-          sum += p0 + p1;
-          pk[h * 16 + c / 2] = pack_bf16x2(p0, p1);
-        }
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[h][c]), c2, nm));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[h][c + 1]), c2, nm));
+            sum += p0 + p1;
+            pk[h * 16 + c / 2] = pack_bf16x2(p0, p1);
+          }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float s0 = __uint_as_float(sr[h][c]), s1 = __uint_as_float(sr[h][c + 1]);
+            const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
+            const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
+            sum += p0 + p1;
+            pk[h * 16 + c / 2] = pack_bf16x2(p0, p1);
+          }
+      }
       l_run = l_run * alpha + sum;
 
       if (j > 0) {  // the previous P V is done: P buffer free, O stable
