@@ -293,9 +293,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       ok = mbar_wait(bar(kBarSFull), j & 1);
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t sr[2][32];
-      tmem_ld32(trow + kColS, sr[0]);
-      tmem_ld32(trow + kColS + 32, sr[1]);
+      uint32_t sr[64];
+      tmem_ld64(trow + kColS, sr);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSFree));
@@ -303,60 +302,61 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       const int kbase = j * kKeys;
       // Tiles below every row's causal limit and inside k_len need no mask (CTA-uniform test);
       // there, with a positive scale, max and exp take the raw scores: p = 2^(s*c - m).
+      // Max and sum use eight partial accumulators to keep dependency chains short.
       const bool full = kbase + kKeys - 1 <= P + q0 && kbase + kKeys <= k_len &&
                         p.qk_scale_log2 > 0.f;
-      float mt = -INFINITY;
+      float part[8];
       if (full) {
-        float mraw = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(sr[u]);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mraw = fmaxf(mraw, __uint_as_float(sr[h][c]));
-        mt = mraw * p.qk_scale_log2;
+        for (int c = 8; c < 64; ++c) part[c & 7] = fmaxf(part[c & 7], __uint_as_float(sr[c]));
       } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int u = 0; u < 8; ++u) part[u] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = kbase + h * 32 + c;
-            const float s = (key <= limit && key < k_len)
-                                ? __uint_as_float(sr[h][c]) * p.qk_scale_log2
-                                : -INFINITY;
-            sr[h][c] = __float_as_uint(s);
-            mt = fmaxf(mt, s);
-          }
+        for (int c = 0; c < 64; ++c) {
+          const int key = kbase + c;
+          const float s = (key <= limit && key < k_len)
+                              ? __uint_as_float(sr[c]) * p.qk_scale_log2
+                              : -INFINITY;
+          sr[c] = __float_as_uint(s);
+          part[c & 7] = fmaxf(part[c & 7], s);
+        }
       }
+      float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                       fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+      if (full) mt *= p.qk_scale_log2;
       const bool resc = mt > m_run + kTauP;
       float alpha = 1.f;
       if (resc) {
         alpha = fast_exp2(m_run - mt);  // 0 when nothing was seen yet
         m_run = mt;
       }
-      float sum = 0.f;
       uint32_t pk[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) part[u] = 0.f;
       if (full) {
         const float c2 = p.qk_scale_log2, nm = -m_run;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[h][c]), c2, nm));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[h][c + 1]), c2, nm));
-            sum += p0 + p1;
-            pk[h * 16 + c / 2] = pack_bf16x2(p0, p1);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), c2, nm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), c2, nm));
+          part[(c >> 1) & 7] += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
       } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float s0 = __uint_as_float(sr[h][c]), s1 = __uint_as_float(sr[h][c + 1]);
-            const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
-            const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
-            sum += p0 + p1;
-            pk[h * 16 + c / 2] = pack_bf16x2(p0, p1);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          const float s0 = __uint_as_float(sr[c]), s1 = __uint_as_float(sr[c + 1]);
+          const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
+          const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
+          part[(c >> 1) & 7] += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
       }
+      const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                        ((part[4] + part[5]) + (part[6] + part[7]));
       l_run = l_run * alpha + sum;
 
       if (j > 0) {  // the previous P V is done: P buffer free, O stable
@@ -406,17 +406,17 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint16_t* orow = p.out + ((int64_t)(q_start + pos) * p.num_q_heads + g * G + r % G) * kHD;
 #pragma unroll 1
-      for (int cc = 0; cc < kHD / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(trow + kColO + cc * 32, o);
-        uint32_t w[16];
+      for (int cc = 0; cc < kHD / 64; ++cc) {
+        uint32_t o[64];
+        tmem_ld64(trow + kColO + cc * 64, o);
+        uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
+        for (int c = 0; c < 32; ++c)
           w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
         if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 8; ++c)
             dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         }
       }
