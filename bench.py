@@ -123,6 +123,22 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows)}
 
 
+def max_over_ranks(x, world, device=None):
+    """The slowest rank's value (timing is taken as the maximum over ranks)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, seconds_max, world):
+    """Whole-job throughput of independent replicas: all ranks' units over the slowest time."""
+    return units_per_rank * world / seconds_max
+
+
 # ------------------------------------------------------------------------------------------------
 # Workload set-up on the device
 # ------------------------------------------------------------------------------------------------
@@ -187,6 +203,78 @@ class DecodeStep:
                 events[l][1].record()
 
 
+class PrefillStep:
+    """The prefix-cache prefill workload: store the new tokens, then varlen causal prefill."""
+
+    def __init__(self, torch, pk, device):
+        self.torch, self.pk = torch, pk
+        self.w = w = W.WORKLOADS["prefix_prefill"]
+        ql = W.prefix_prefill_suffix_lengths(w.num_seqs)
+        c = W.prefix_prefill_case(w.seed, w.num_seqs, 1024, 100, 1024, w.num_q_heads,
+                                  w.num_kv_heads, w.head_dim, w.block_size, suffix_lens=ql)
+        self.case = c
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(  # noqa
+            torch.bfloat16).to(device)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)  # noqa
+        self.q, self.k, self.v = bf(c.q), bf(c.k), bf(c.v)
+        self.kc, self.vc = bf(c.k_cache), bf(c.v_cache)
+        self.cu_q, self.cu_k = i32(c.cu_seqlens_q), i32(c.cu_seqlens_k)
+        self.bt, self.slots = i32(c.block_tables), i32(c.slot_mapping)
+        self.out = torch.empty_like(self.q)
+        self.max_q = int(c.q_lens.max())
+        qn = c.q_lens.astype(np.float64)
+        pre = (c.k_lens - c.q_lens).astype(np.float64)
+        pairs = float(np.sum(qn * pre + qn * (qn + 1) / 2))  # (query, key) pairs under the mask
+        self.flops = 4.0 * w.head_dim * w.num_q_heads * pairs   # QK^T and PV, 2 flops per MAC
+        self.tokens = int(qn.sum())
+
+    def store(self):
+        self.pk.kv_store(self.k, self.v, self.slots, self.kc, self.vc)
+
+    def prefill(self):
+        self.pk.paged_prefill(self.q, self.k, self.v, self.cu_q, self.cu_k, self.bt,
+                              self.case.scale, k_cache=self.kc, v_cache=self.vc, out=self.out,
+                              max_seqlen_q=self.max_q)
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1800.0, "fallback"
+
+
+def prefill_arm(args, torch, pk, device):
+    """--workload prefix_prefill: TFLOP/s of the prefill kernel (a component, not the headline)."""
+    ps = PrefillStep(torch, pk, device)
+    for _ in range(args.warmup):
+        ps.store()
+        ps.prefill()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        ps.store()
+        a.record()
+        ps.prefill()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    peak, kind = measured_tensor_peak()
+    tf = ps.flops / (ms / 1e3) / 1e12
+    line = {"metric": "prefix-cache prefill TFLOP/s (causal, algorithmic)", "value": tf,
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "accumulate": "fp32",
+            "data": "synthetic", "config": {"workload": "prefix_prefill", "num_seqs": 64,
+                                            "new_tokens": ps.tokens, "prefix": 1024},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "peak_source": kind},
+            "device_error_flags": pk.get_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------------------------------------
 # CPU oracle arm
 # ------------------------------------------------------------------------------------------------
@@ -200,24 +288,34 @@ def oracle_sample_case(name, n_seqs):
                                 w.block_size, 0, 0, context_lens=ctx)
 
 
-def time_oracle(name, target_s=12.0, max_seqs=256):
-    """Time the oracle (store + decode of one layer) on a sample sized to about target_s."""
+def time_oracle(name, target_s=10.0, max_seqs=1024):
+    """Time the oracle (store + decode of one layer) on a host sample: as many sequences as make
+    one run take about a second (at most one layer's worth), repeated to about target_s."""
     import oracle
     orc = oracle.default()
     w = W.WORKLOADS[name]
     n = 8
-    while True:
-        case = oracle_sample_case(name, n)
+
+    def one(case):
         t0 = time.perf_counter()
         kc, vc, _ = orc.kv_store(case.k_new, case.v_new, case.slot_mapping, case.k_cache,
                                  case.v_cache)
         orc.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale)
-        dt = time.perf_counter() - t0
-        if dt >= target_s / 4 or n >= max_seqs:
+        return time.perf_counter() - t0
+
+    while True:
+        case = oracle_sample_case(name, n)
+        dt = one(case)
+        if dt >= 1.0 or n >= max_seqs:
             break
-        n = min(max_seqs, max(n + 1, int(n * target_s / 4 / max(dt, 1e-3))))
+        n = min(max_seqs, max(n + 1, int(n * 1.2 / max(dt, 1e-3))))
+    runs, total = [dt], dt
+    while total < target_s:
+        runs.append(one(case))
+        total += runs[-1]
+    dt = sum(runs) / len(runs)
     kv = int(case.context_lens.sum()) * w.kv_bytes_per_token
-    return dict(n_seqs=n, seconds=dt, kv_bytes=kv, cores=orc.max_threads(),
+    return dict(n_seqs=n, seconds=dt, runs=len(runs), kv_bytes=kv, cores=orc.max_threads(),
                 gbs=kv / dt / 1e9, tokens_per_s=n / (dt * w.num_layers))
 
 
@@ -228,7 +326,7 @@ def reference_arm(args):
     import oracle
     orc = oracle.default()
     w = W.WORKLOADS[args.workload]
-    probe = time_oracle(args.workload, target_s=4.0, max_seqs=64)
+    probe = time_oracle(args.workload, target_s=2.0, max_seqs=64)
     n = probe["n_seqs"]
     case = oracle_sample_case(args.workload, n)
     times = []
@@ -298,6 +396,8 @@ def main():
     if gpu_uuid and not gpu_uuid.startswith("GPU-"):
         gpu_uuid = "GPU-" + gpu_uuid
 
+    if args.workload == "prefix_prefill":
+        return prefill_arm(args, torch, pk, device)
     step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
                       num_layers=args.layers)
     reduced = bool(args.num_seqs or args.layers)
@@ -307,12 +407,8 @@ def main():
         if world > 1:
             torch.distributed.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    def ranks_max(x):
+        return max_over_ranks(x, world, device)
 
     # ---- warm-up, then the timed region ----
     for _ in range(args.warmup):
@@ -331,16 +427,16 @@ def main():
         stop.record()
         torch.cuda.synchronize()
     barrier()
-    ms = max_over_ranks(start.elapsed_time(stop) / args.steps)
+    ms = ranks_max(start.elapsed_time(stop) / args.steps)
     decode_ms = [e[0].elapsed_time(e[1]) for s in evs for e in s]
-    decode_ms_mean = max_over_ranks(sum(decode_ms) / len(decode_ms))
+    decode_ms_mean = ranks_max(sum(decode_ms) / len(decode_ms))
     flags = pk.get_device_error()
     if flags:
         log(f"[bench] device error flags {flags:#x}")
 
     kv_step = step.kv_bytes_per_layer * step.L
-    value = kv_step * world / (ms / 1e3) / 1e9
-    tokens_per_s = step.B * world / (ms / 1e3)
+    value = job_throughput(kv_step, ms / 1e3, world) / 1e9
+    tokens_per_s = job_throughput(step.B, ms / 1e3, world)
     peak, peak_kind = measured_peaks()
     achieved = step.kv_bytes_per_layer / (decode_ms_mean / 1e3) / 1e9
     traffic = profiled_traffic("paged_decode_qwen3_8b",
@@ -359,19 +455,35 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_bt, h_ctx, h_sl])
         d2h = sum(x.numel() * x.element_size() for x in h_out)
 
+        # Copies overlap compute: layer l's inputs are copied in on one stream while earlier
+        # layers compute, and layer l's output is copied out on another as soon as it is done.
+        main = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(step.L)]
+        ev_done = [torch.cuda.Event() for _ in range(step.L)]
+
         def e2e_step():
-            step.bt_dev.copy_(h_bt, non_blocking=True)
-            step.ctx_dev.copy_(h_ctx, non_blocking=True)
-            step.slots_dev.copy_(h_sl, non_blocking=True)
+            s_in.wait_stream(main)  # buffers of the previous step are no longer in use
+            with torch.cuda.stream(s_in):
+                step.bt_dev.copy_(h_bt, non_blocking=True)
+                step.ctx_dev.copy_(h_ctx, non_blocking=True)
+                step.slots_dev.copy_(h_sl, non_blocking=True)
+                for l in range(step.L):
+                    step.q[l].copy_(h_q[l], non_blocking=True)
+                    step.k_new[l].copy_(h_k[l], non_blocking=True)
+                    step.v_new[l].copy_(h_v[l], non_blocking=True)
+                    ev_in[l].record(s_in)
             for l in range(step.L):
-                step.q[l].copy_(h_q[l], non_blocking=True)
-                step.k_new[l].copy_(h_k[l], non_blocking=True)
-                step.v_new[l].copy_(h_v[l], non_blocking=True)
+                main.wait_event(ev_in[l])
                 kc, vc = step.pools[l % step.n_pools]
                 pk.kv_store(step.k_new[l], step.v_new[l], step.slots_dev, kc, vc)
                 pk.paged_decode(step.q[l], kc, vc, step.bt_dev, step.ctx_dev, step.scale,
                                 out=step.out[l], plan=step.plan, workspace=step.ws)
-                h_out[l].copy_(step.out[l], non_blocking=True)
+                ev_done[l].record(main)
+                s_out.wait_event(ev_done[l])
+                with torch.cuda.stream(s_out):
+                    h_out[l].copy_(step.out[l], non_blocking=True)
+            main.wait_stream(s_out)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -384,7 +496,7 @@ def main():
         e1.record()
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        e2e_ms = ranks_max(e0.elapsed_time(e1) / args.steps)
         e2e = {"value": kv_step * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                "ms_per_step": e2e_ms, "decode_tokens_per_s": step.B * world / (e2e_ms / 1e3),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -398,7 +510,7 @@ def main():
         r = time_oracle(args.workload)
         cpu = {"value": r["gbs"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['n_seqs']} sequences x 1 layer (store + decode), "
-                         f"{r['seconds']:.1f} s, KV GB/s of the sample",
+                         f"{r['runs']} runs of {r['seconds']:.2f} s, KV GB/s of the sample",
                "decode_tokens_per_s": r["tokens_per_s"]}
 
     if rank == 0:
@@ -477,6 +589,17 @@ def secondary_measurements(torch, pk, device, main_step):
         del layer
     except Exception as e:  # report, do not hide
         res["long_splitk_decode"] = {"error": repr(e)}
+    try:
+        ps = PrefillStep(torch, pk, device)
+        ps.store()
+        ms = timed(ps.prefill)
+        peak, _ = measured_tensor_peak()
+        tf = ps.flops / (ms / 1e3) / 1e12
+        res["prefix_prefill"] = {"ms": ms, "TFLOP/s": tf, "frac_of_bf16_peak": tf / peak,
+                                 "new_tokens": ps.tokens}
+        del ps
+    except Exception as e:
+        res["prefix_prefill"] = {"error": repr(e)}
     try:
         layer = _decode_layer("qwen3_0p6b_decode", torch, device)
         ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],

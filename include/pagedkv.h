@@ -197,6 +197,14 @@ PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16
  */
 PKV_API int pkv_get_device_error(int32_t* flags);
 
+/*
+ * Diagnostic for the failure-detection path: launches one CTA that waits on a barrier nothing will
+ * ever complete. The wait is bounded like every pipeline wait in the kernels: after one second it
+ * gives up, sets PKV_DEVERR_TIMEOUT in the device error word and the CTA exits, so the context
+ * stays usable. Enqueued on `stream`; read the result with pkv_get_device_error().
+ */
+PKV_API int pkv_selftest_bounded_wait(void* stream);
+
 /* Text for a PKV_* status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 

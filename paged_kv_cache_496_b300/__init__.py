@@ -59,8 +59,8 @@ class PagedKVError(RuntimeError):
 
 def _load():
     if not os.path.exists(LIBRARY):
-        raise ImportError(f"{LIBRARY} is missing: build it with `python -m "
-                          "paged_kv_cache_496_b300.build` (nvcc, sm_103a)")
+        raise ImportError(f"{LIBRARY} is missing: build it with `python "
+                          "paged_kv_cache_496_b300/build.py` (nvcc, sm_103a)")
     L = ctypes.CDLL(LIBRARY)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     L.pkv_kv_store.restype = ctypes.c_int
@@ -73,6 +73,8 @@ def _load():
     L.pkv_paged_prefill.restype = ctypes.c_int
     L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp,
                                     CacheDesc, i32, f32, vp, vp]
+    L.pkv_selftest_bounded_wait.restype = ctypes.c_int
+    L.pkv_selftest_bounded_wait.argtypes = [vp]
     L.pkv_get_device_error.restype = ctypes.c_int
     L.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -234,3 +236,9 @@ def get_device_error() -> int:
     v = ctypes.c_int32(0)
     _check(lib.pkv_get_device_error(ctypes.byref(v)))
     return int(v.value)
+
+
+def selftest_bounded_wait(stream=None):
+    """Run the bounded-wait diagnostic (about one second); returns the device error word."""
+    _check(lib.pkv_selftest_bounded_wait(_stream_ptr(stream)))
+    return get_device_error()

@@ -1,6 +1,7 @@
 """Build libpagedkv.so (the C-ABI library) for sm_103a with nvcc, in-tree.
 
-`python -m paged_kv_cache_496_b300.build` or `build()`. The library is written next to this file.
+Run `python paged_kv_cache_496_b300/build.py` (as a script: importing the package would load the
+library it is about to build). The library is written next to this file.
 """
 from __future__ import annotations
 

@@ -134,6 +134,18 @@ int check_heads(int num_q_heads, int num_kv_heads) {
 
 constexpr int32_t kAutoSplitFloor = 512;
 
+// One CTA waits on an mbarrier that nothing ever completes, with the same bounded wait the
+// kernels' pipelines use; the wait gives up after its time limit and reports a timeout.
+__global__ void bounded_wait_selftest_kernel(int* flags) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(smem_addr(&bar), 0)) raise_flag(flags, PKV_DEVERR_TIMEOUT);
+}
+
 int32_t round_up(int64_t x, int64_t q) { return (int32_t)((x + q - 1) / q * q); }
 
 }  // namespace
@@ -172,6 +184,17 @@ int pkv_get_device_error(int32_t* flags) {
   e = cudaMemcpy(d.flags, &zero, sizeof zero, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
   *flags = v;
+  return PKV_OK;
+}
+
+int pkv_selftest_bounded_wait(void* stream) {
+  g_last_error[0] = 0;
+  DeviceInfo d;
+  int st = device_info(&d);
+  if (st != PKV_OK) return st;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d.flags);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return PKV_OK;
 }
 
