@@ -579,6 +579,18 @@ def secondary_measurements(torch, pk, device, main_step):
     ms = timed(lambda: pk.kv_store(kn, kn, slots, kc, vc))
     res["kv_store_35968_tokens"] = {"ms": ms, "GB/s": 2 * 2 * T * row / ms / 1e6}
 
+    # whole-block moves on the decode pool: 512 copy-on-write copies and a 512-block swap-out
+    perm = torch.from_numpy(W.rng_for(3, 500).permutation(main_step.nb)[:1024].astype(np.int32))
+    pairs = perm.view(512, 2).contiguous().to(device)
+    ids = perm[:512].contiguous().to(device)
+    blk_bytes = 256 * main_step.w.num_kv_heads * main_step.w.head_dim * 2 * 2  # K and V
+    ms = timed(lambda: pk.copy_blocks(kc, vc, pairs))
+    res["copy_blocks_512"] = {"ms": ms, "GB/s": 2 * 512 * blk_bytes / ms / 1e6}
+    gk, gv = pk.gather_blocks(kc, vc, ids)
+    ms = timed(lambda: pk.gather_blocks(kc, vc, ids, out_k=gk, out_v=gv))
+    res["gather_blocks_512"] = {"ms": ms, "GB/s": 2 * 512 * blk_bytes / ms / 1e6}
+    del gk, gv
+
     # long-context split decode (one layer)
     try:
         layer = _decode_layer("long_splitk_decode", torch, device)
@@ -601,6 +613,10 @@ def secondary_measurements(torch, pk, device, main_step):
     except Exception as e:
         res["prefix_prefill"] = {"error": repr(e)}
     try:
+        res["mixed_prefill_decode"] = _mixed_batch(torch, pk, device, timed)
+    except Exception as e:
+        res["mixed_prefill_decode"] = {"error": repr(e)}
+    try:
         layer = _decode_layer("qwen3_0p6b_decode", torch, device)
         ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
                                            layer["ctx"], layer["scale"], out=layer["out"],
@@ -610,6 +626,44 @@ def secondary_measurements(torch, pk, device, main_step):
     except Exception as e:
         res["qwen3_0p6b_decode_layer"] = {"error": repr(e)}
     return res
+
+
+def _mixed_batch(torch, pk, device, timed):
+    """One varlen call mixing 960 decode rows (one new token each) and 64 prefill chunks of 256
+    tokens after a 512-token cached prefix, at Qwen3-8B head geometry, block size 256."""
+    import paged_kv_cache_496_b300 as pkm
+    rng = W.rng_for(7, 400)
+    n_dec, n_pre = 960, 64
+    dec_ctx = W.decode_context_lengths(rng, n_dec)
+    ql = np.concatenate([np.ones(n_dec, np.int32), np.full(n_pre, 256, np.int32)])
+    prefix = np.concatenate([dec_ctx - 1, np.full(n_pre, 512, np.int32)]).astype(np.int32)
+    kl = ql + prefix
+    BS, Hq, Hkv, D = 256, 32, 8, 128
+    bt, nb = W.place_blocks(rng, kl, BS)
+    mk = lambda shape, s: W.fill_normal_bf16_(  # noqa: E731
+        torch.empty(shape, dtype=torch.bfloat16, device=device), 7, s)
+    kc, vc = mk((nb, BS, Hkv, D), 1), mk((nb, BS, Hkv, D), 2)
+    T = int(ql.sum())
+    q, k, v = mk((T, Hq, D), 3), mk((T, Hkv, D), 4), mk((T, Hkv, D), 5)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)  # noqa
+    cu_q = i32(np.concatenate([[0], np.cumsum(ql)]))
+    cu_k = i32(np.concatenate([[0], np.cumsum(kl)]))
+    seq = np.concatenate([np.full(n, b) for b, n in enumerate(ql)])
+    pos = np.concatenate([prefix[b] + np.arange(n) for b, n in enumerate(ql)])
+    slots = i32(W.slots_for_positions(bt, seq, pos, BS))
+    btd = i32(bt)
+    out = torch.empty_like(q)
+    pkm.kv_store(k, v, slots, kc, vc)
+
+    def call():
+        pkm.paged_prefill(q, k, v, cu_q, cu_k, btd, 1 / np.sqrt(D), k_cache=kc, v_cache=vc,
+                          out=out, max_seqlen_q=256)
+    ms = timed(call)
+    qn, pre = ql.astype(np.float64), prefix.astype(np.float64)
+    flops = 4.0 * D * Hq * float(np.sum(qn * pre + qn * (qn + 1) / 2))
+    kv = float(kl.sum()) * Hkv * D * 4
+    return {"ms": ms, "TFLOP/s": flops / ms / 1e9, "KV GB/s": kv / ms / 1e6,
+            "rows": "960 decode + 64 x 256 prefill"}
 
 
 def _decode_layer(name, torch, device):

@@ -136,6 +136,30 @@ PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const u
                      uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Whole-block moves ["nano-vllm 深度分析报告", section "解法哲学": swap (CPU offload) and
+ * copy-on-write are the block-level features Nano-vLLM leaves out and vLLM keeps].
+ * A block of one cache is block_size * num_kv_heads * head_dim bf16, contiguous; every call moves
+ * the K and the V block alike. Block ids outside [0, num_blocks) are skipped and flagged
+ * (PKV_DEVERR_BAD_BLOCK). n == 0 is a no-op.
+ *
+ * pkv_copy_blocks: copy-on-write. For i in [0, n): block pairs[2i+1] := block pairs[2i].
+ *   pairs   device, [n, 2] int32 (source, destination). A block that is a destination must not
+ *           also be a source in the same call (the result would be unspecified).
+ * pkv_gather_blocks: swap out. out_k[i] := k_cache[ids[i]], out_v[i] := v_cache[ids[i]].
+ *   ids     device, [n] int32;  out_k, out_v  device, [n, block_size, num_kv_heads, head_dim]
+ * pkv_scatter_blocks: swap in. k_cache[ids[i]] := in_k[i], v_cache[ids[i]] := in_v[i].
+ *   ids must be distinct.
+ */
+PKV_API int pkv_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, pkv_cache_desc cache,
+                            const int32_t* pairs, int32_t n, void* stream);
+PKV_API int pkv_gather_blocks(const uint16_t* k_cache, const uint16_t* v_cache,
+                              pkv_cache_desc cache, const int32_t* ids, int32_t n,
+                              uint16_t* out_k, uint16_t* out_v, void* stream);
+PKV_API int pkv_scatter_blocks(const uint16_t* in_k, const uint16_t* in_v, const int32_t* ids,
+                               int32_t n, uint16_t* k_cache, uint16_t* v_cache,
+                               pkv_cache_desc cache, void* stream);
+
+/*
  * Paged decode without any device allocation by the caller (no counterpart in the source pages:
  * it exists for callers of this library that cannot allocate device memory).
  * Some callers cannot call cudaMalloc for the decode workspace: a process that has given all of

@@ -61,6 +61,16 @@ class Oracle:
                                              ctypes.c_int32, ctypes.c_double, _f64p,
                                              ctypes.c_int32]
         lib.oracle_max_threads.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        lib.oracle_copy_blocks.restype = ctypes.c_int32
+        lib.oracle_copy_blocks.argtypes = [_u16p, _u16p, ctypes.c_int32, i64, _i32p,
+                                           ctypes.c_int32]
+        lib.oracle_gather_blocks.restype = ctypes.c_int32
+        lib.oracle_gather_blocks.argtypes = [_u16p, _u16p, ctypes.c_int32, i64, _i32p,
+                                             ctypes.c_int32, _u16p, _u16p]
+        lib.oracle_scatter_blocks.restype = ctypes.c_int32
+        lib.oracle_scatter_blocks.argtypes = [_u16p, _u16p, _i32p, ctypes.c_int32, _u16p, _u16p,
+                                              ctypes.c_int32, i64]
         self.lib = lib
 
     def max_threads(self) -> int:
@@ -140,6 +150,40 @@ class Oracle:
         if rc:
             raise IndexError("block table walk left the pool")
         return out
+
+
+    # -- Whole-block moves ----------------------------------------------------------------------
+    def copy_blocks(self, k_cache, v_cache, pairs):
+        """Return (k_cache', v_cache', skipped) after copying pairs[i,0] -> pairs[i,1]."""
+        kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+        vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+        pr = _c(pairs, np.int32)
+        bad = self.lib.oracle_copy_blocks(_ptr(kc, _u16p), _ptr(vc, _u16p), kc.shape[0],
+                                          int(np.prod(kc.shape[1:])), _ptr(pr, _i32p),
+                                          pr.shape[0])
+        return kc, vc, int(bad)
+
+    def gather_blocks(self, k_cache, v_cache, ids):
+        kc = _c(k_cache, np.uint16)
+        vc = _c(v_cache, np.uint16)
+        ids = _c(ids, np.int32)
+        ok = np.zeros((len(ids),) + kc.shape[1:], np.uint16)
+        ov = np.zeros_like(ok)
+        bad = self.lib.oracle_gather_blocks(_ptr(kc, _u16p), _ptr(vc, _u16p), kc.shape[0],
+                                            int(np.prod(kc.shape[1:])), _ptr(ids, _i32p),
+                                            len(ids), _ptr(ok, _u16p), _ptr(ov, _u16p))
+        return ok, ov, int(bad)
+
+    def scatter_blocks(self, in_k, in_v, ids, k_cache, v_cache):
+        kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+        vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+        ik = _c(in_k, np.uint16)
+        iv = _c(in_v, np.uint16)
+        ids = _c(ids, np.int32)
+        bad = self.lib.oracle_scatter_blocks(_ptr(ik, _u16p), _ptr(iv, _u16p), _ptr(ids, _i32p),
+                                             len(ids), _ptr(kc, _u16p), _ptr(vc, _u16p),
+                                             kc.shape[0], int(np.prod(kc.shape[1:])))
+        return kc, vc, int(bad)
 
 
 _default: Optional[Oracle] = None

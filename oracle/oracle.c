@@ -255,3 +255,61 @@ int oracle_paged_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v
   }
   return status;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Whole-block moves ["nano-vllm 深度分析报告", section "解法哲学": swap (CPU offload) and
+ * copy-on-write act on whole physical blocks]. block_elems = block_size * Hkv * D values.
+ * Each returns the number of entries skipped because a block id was outside [0, num_blocks).
+ * ------------------------------------------------------------------------------------------- */
+int32_t oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
+                           int64_t block_elems, const int32_t *pairs, int32_t n) {
+  int32_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      ++bad;
+      continue;
+    }
+    memcpy(k_cache + dst * block_elems, k_cache + src * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+    memcpy(v_cache + dst * block_elems, v_cache + src * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+  }
+  return bad;
+}
+
+int32_t oracle_gather_blocks(const uint16_t *k_cache, const uint16_t *v_cache, int32_t num_blocks,
+                             int64_t block_elems, const int32_t *ids, int32_t n, uint16_t *out_k,
+                             uint16_t *out_v) {
+  int32_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t blk = ids[i];
+    if (blk < 0 || blk >= num_blocks) {
+      ++bad;
+      continue;
+    }
+    memcpy(out_k + i * block_elems, k_cache + blk * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+    memcpy(out_v + i * block_elems, v_cache + blk * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+  }
+  return bad;
+}
+
+int32_t oracle_scatter_blocks(const uint16_t *in_k, const uint16_t *in_v, const int32_t *ids,
+                              int32_t n, uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
+                              int64_t block_elems) {
+  int32_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t blk = ids[i];
+    if (blk < 0 || blk >= num_blocks) {
+      ++bad;
+      continue;
+    }
+    memcpy(k_cache + blk * block_elems, in_k + i * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+    memcpy(v_cache + blk * block_elems, in_v + i * block_elems,
+           (size_t)block_elems * sizeof(uint16_t));
+  }
+  return bad;
+}

@@ -73,6 +73,12 @@ def _load():
     L.pkv_paged_prefill.restype = ctypes.c_int
     L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp,
                                     CacheDesc, i32, f32, vp, vp]
+    L.pkv_copy_blocks.restype = ctypes.c_int
+    L.pkv_copy_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, vp]
+    L.pkv_gather_blocks.restype = ctypes.c_int
+    L.pkv_gather_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, vp, vp, vp]
+    L.pkv_scatter_blocks.restype = ctypes.c_int
+    L.pkv_scatter_blocks.argtypes = [vp, vp, vp, i32, vp, vp, CacheDesc, vp]
     L.pkv_selftest_bounded_wait.restype = ctypes.c_int
     L.pkv_selftest_bounded_wait.argtypes = [vp]
     L.pkv_get_device_error.restype = ctypes.c_int
@@ -242,3 +248,42 @@ def selftest_bounded_wait(stream=None):
     """Run the bounded-wait diagnostic (about one second); returns the device error word."""
     _check(lib.pkv_selftest_bounded_wait(_stream_ptr(stream)))
     return get_device_error()
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """Copy-on-write: block pairs[i, 1] := block pairs[i, 0] in both caches."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(pairs, "pairs", torch.int32, 2)
+    if pairs.shape[1] != 2 or k_cache.shape != v_cache.shape:
+        raise ValueError("pairs must be [n, 2] and the caches alike")
+    _check(lib.pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), _cache_desc(k_cache),
+                               pairs.data_ptr(), pairs.shape[0], _stream_ptr(stream)))
+
+
+def gather_blocks(k_cache, v_cache, ids, out_k=None, out_v=None, stream=None):
+    """Swap out: returns (out_k, out_v) [n, block_size, Hkv, D] holding blocks ids of each cache."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(ids, "ids", torch.int32, 1)
+    shape = (ids.shape[0],) + tuple(k_cache.shape[1:])
+    out_k = torch.empty(shape, dtype=torch.bfloat16, device=k_cache.device) if out_k is None \
+        else out_k
+    out_v = torch.empty(shape, dtype=torch.bfloat16, device=k_cache.device) if out_v is None \
+        else out_v
+    _need(out_k, "out_k", torch.bfloat16, 4)
+    _need(out_v, "out_v", torch.bfloat16, 4)
+    _check(lib.pkv_gather_blocks(k_cache.data_ptr(), v_cache.data_ptr(), _cache_desc(k_cache),
+                                 ids.data_ptr(), ids.shape[0], out_k.data_ptr(),
+                                 out_v.data_ptr(), _stream_ptr(stream)))
+    return out_k, out_v
+
+
+def scatter_blocks(in_k, in_v, ids, k_cache, v_cache, stream=None):
+    """Swap in: k_cache[ids[i]] := in_k[i], v_cache[ids[i]] := in_v[i]."""
+    for t, name in ((in_k, "in_k"), (in_v, "in_v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, name, torch.bfloat16, 4)
+    _need(ids, "ids", torch.int32, 1)
+    _check(lib.pkv_scatter_blocks(in_k.data_ptr(), in_v.data_ptr(), ids.data_ptr(),
+                                  ids.shape[0], k_cache.data_ptr(), v_cache.data_ptr(),
+                                  _cache_desc(k_cache), _stream_ptr(stream)))

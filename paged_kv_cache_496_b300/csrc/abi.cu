@@ -219,6 +219,46 @@ int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* slot_mappi
   return PKV_OK;
 }
 
+int block_move(int mode, uint16_t* k_cache, uint16_t* v_cache, const pkv_cache_desc& cache,
+               const int32_t* ids, int32_t n, uint16_t* buf_k, uint16_t* buf_v, void* stream) {
+  g_last_error[0] = 0;
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (n < 0) return fail(PKV_ERR_INVALID_ARG, "n %d < 0", n);
+  if (n == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !ids || (mode != 0 && (!buf_k || !buf_v)))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_cache) || !aligned16(v_cache) ||
+      (mode != 0 && (!aligned16(buf_k) || !aligned16(buf_v))))
+    return fail(PKV_ERR_INVALID_ARG, "caches and buffers must be 16-byte aligned");
+  DeviceInfo d;
+  st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_block_move(mode, k_cache, v_cache, ids, n, cache, buf_k, buf_v,
+                                    d.num_sms, d.flags, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block move launch");
+  return PKV_OK;
+}
+
+int pkv_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, pkv_cache_desc cache,
+                    const int32_t* pairs, int32_t n, void* stream) {
+  return block_move(0, k_cache, v_cache, cache, pairs, n, nullptr, nullptr, stream);
+}
+
+int pkv_gather_blocks(const uint16_t* k_cache, const uint16_t* v_cache, pkv_cache_desc cache,
+                      const int32_t* ids, int32_t n, uint16_t* out_k, uint16_t* out_v,
+                      void* stream) {
+  return block_move(1, const_cast<uint16_t*>(k_cache), const_cast<uint16_t*>(v_cache), cache,
+                    ids, n, out_k, out_v, stream);
+}
+
+int pkv_scatter_blocks(const uint16_t* in_k, const uint16_t* in_v, const int32_t* ids, int32_t n,
+                       uint16_t* k_cache, uint16_t* v_cache, pkv_cache_desc cache,
+                       void* stream) {
+  return block_move(2, k_cache, v_cache, cache, ids, n, const_cast<uint16_t*>(in_k),
+                    const_cast<uint16_t*>(in_v), stream);
+}
+
 int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
                          int32_t max_context_len, int32_t split_tokens_hint,
                          pkv_decode_plan* plan) {

@@ -48,6 +48,13 @@ struct DecodeArgs {
   int* flags;
 };
 
+// Whole-block moves: mode 0 copies (src, dst) pairs inside the caches, mode 1 gathers blocks
+// into buf_k/buf_v, mode 2 scatters them back from buf_k/buf_v.
+cudaError_t launch_block_move(int mode, uint16_t* k_cache, uint16_t* v_cache,
+                              const int32_t* ids, int32_t n, const pkv_cache_desc& cache,
+                              uint16_t* buf_k, uint16_t* buf_v, int num_sms, int* flags,
+                              cudaStream_t stream);
+
 // Rows of the K/V TMA box the decode kernel expects (tile tokens, or the block size if smaller).
 int decode_box_rows(int head_dim, int group, int block_size);
 

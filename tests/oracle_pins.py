@@ -383,6 +383,38 @@ def pin_prefill_shared_vs_duplicated_prefix(orc):
     assert np.array_equal(oa, ob), "shared prefix blocks and duplicated copies differ"
 
 
+# ------------------------------------------------------------------------------------------------
+# Whole-block moves
+# ------------------------------------------------------------------------------------------------
+
+
+def pin_block_moves_match_numpy(orc):
+    rng = W.rng_for(41, 0)
+    NB, BS, Hkv, D = 12, 4, 2, 8
+    kc = W.normal_bf16(rng, (NB, BS, Hkv, D))
+    vc = W.normal_bf16(rng, (NB, BS, Hkv, D))
+    pairs = np.array([[3, 7], [0, 11], [5, 2], [-1, 4], [6, 12]], np.int32)
+    k2, v2, bad = orc.copy_blocks(kc, vc, pairs)
+    assert bad == 2, "two pairs leave the pool"
+    rk, rv = kc.copy(), vc.copy()
+    ok = pairs[:3]
+    rk[ok[:, 1]] = kc[ok[:, 0]]
+    rv[ok[:, 1]] = vc[ok[:, 0]]
+    assert np.array_equal(k2, rk) and np.array_equal(v2, rv), "copy-on-write differs"
+    ids = np.array([9, 1, 4, 4], np.int32)
+    gk, gv, bad = orc.gather_blocks(kc, vc, ids)
+    assert bad == 0 and np.array_equal(gk, kc[ids]) and np.array_equal(gv, vc[ids])
+    dst = np.array([0, 2, 10, 6], np.int32)
+    sk, sv, bad = orc.scatter_blocks(gk, gv, dst, kc, vc)
+    rk, rv = kc.copy(), vc.copy()
+    rk[dst] = gk
+    rv[dst] = gv
+    assert bad == 0 and np.array_equal(sk, rk) and np.array_equal(sv, rv), "scatter differs"
+    # swap out then swap in elsewhere is a permutation of placement: gathering again gives back
+    back, _, _ = orc.gather_blocks(sk, sv, dst)
+    assert np.array_equal(back, kc[ids])
+
+
 ALL_PINS = [
     pin_store_matches_numpy_scatter,
     pin_store_padding_and_invalid,
@@ -399,4 +431,5 @@ ALL_PINS = [
     pin_prefill_prefix_matches_masked_sdpa,
     pin_prefill_row_equals_decode,
     pin_prefill_shared_vs_duplicated_prefix,
+    pin_block_moves_match_numpy,
 ]

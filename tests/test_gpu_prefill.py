@@ -151,3 +151,54 @@ def test_full_prefix_prefill_workload(orc):
         ref = _oracle(orc, sub)
         rows = slice(int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1]))
         assert_attn_close(out[rows], ref, what=f"full workload seq {b}")
+
+
+def _prefill_call(q, k, v, cu_q, cu_k, bt, scale, kc, vc):
+    out = pk.paged_prefill(dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_i32(cu_q), dev_i32(cu_k),
+                           dev_i32(bt), scale, k_cache=kc, v_cache=vc)
+    assert pk.get_device_error() == 0
+    return out
+
+
+def test_chunked_prefill_equals_one_shot(orc):
+    """A prompt prefilled in two chunks (the second sees the first as cached prefix) gives the
+    same rows as one prefill of the whole prompt."""
+    case = W.prefix_prefill_case(68, 1, 256, 0, 0, 32, 8, 128, 64, suffix_lens=np.array([300]))
+    kc, vc = dev_bf16(case.k_cache), dev_bf16(case.v_cache)
+    pk.kv_store(dev_bf16(case.k), dev_bf16(case.v), dev_i32(case.slot_mapping), kc, vc)
+    whole = _prefill_call(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
+                          case.block_tables, case.scale, kc, vc)
+    a = 120
+    first = _prefill_call(case.q[:a], case.k[:a], case.v[:a], np.array([0, a]),
+                          np.array([0, 256 + a]), case.block_tables, case.scale, kc, vc)
+    second = _prefill_call(case.q[a:], case.k[a:], case.v[a:], np.array([0, 300 - a]),
+                           np.array([0, 556]), case.block_tables, case.scale, kc, vc)
+    chunked = torch.cat([first, second])
+    assert (chunked.float() - whole.float()).abs().max().item() <= TOL
+    assert_attn_close(chunked, _oracle(orc, case), what="chunked prefill")
+
+
+def test_mixed_decode_and_prefill_batch(orc):
+    """Decode rows (one new token) and prefill chunks in one varlen call."""
+    rng = W.rng_for(69, 0)
+    ql = np.array([1, 1, 200, 1, 64, 1, 129], np.int32)
+    prefix = np.array([300, 1000, 0, 17, 512, 1, 255], np.int32)
+    BS, Hq, Hkv, D = 16, 32, 8, 128
+    kl = ql + prefix
+    bt, nb = W.place_blocks(rng, kl, BS)
+    kc = W.normal_bf16(rng, (nb, BS, Hkv, D))
+    vc = W.normal_bf16(rng, (nb, BS, Hkv, D))
+    T = int(ql.sum())
+    q = W.normal_bf16(rng, (T, Hq, D))
+    k = W.normal_bf16(rng, (T, Hkv, D))
+    v = W.normal_bf16(rng, (T, Hkv, D))
+    cu_q = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(kl)]).astype(np.int32)
+    seq = np.concatenate([np.full(n, b) for b, n in enumerate(ql)])
+    pos = np.concatenate([prefix[b] + np.arange(n) for b, n in enumerate(ql)])
+    slots = W.slots_for_positions(bt, seq, pos, BS)
+    kcd, vcd = dev_bf16(kc), dev_bf16(vc)
+    pk.kv_store(dev_bf16(k), dev_bf16(v), dev_i32(slots), kcd, vcd)
+    out = _prefill_call(q, k, v, cu_q, cu_k, bt, 1 / np.sqrt(D), kcd, vcd)
+    ref = orc.paged_prefill(q, k, v, cu_q, cu_k, bt, kc, vc, 1 / np.sqrt(D))
+    assert_attn_close(out, ref, what="mixed batch")

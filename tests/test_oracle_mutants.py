@@ -30,6 +30,10 @@ MUTANTS = {
     "prefix_keys_from_new_rows": ("bad |= oracle_gather_head(k_cache, num_blocks, block_size, num_kv_heads, head_dim, bt_row,\n                                P, g, K);",
                                   "bad |= oracle_gather_head(v_cache, num_blocks, block_size, num_kv_heads, head_dim, bt_row,\n                                P, g, K);"),
     "max_not_tracked": ("if (s[j] > m) m = s[j];", "if (s[j] < m) m = s[j];"),
+    "cow_copies_backwards": ("memcpy(k_cache + dst * block_elems, k_cache + src * block_elems,",
+                             "memcpy(k_cache + src * block_elems, k_cache + dst * block_elems,"),
+    "gather_reads_v_for_k": ("memcpy(out_k + i * block_elems, k_cache + blk * block_elems,",
+                             "memcpy(out_k + i * block_elems, v_cache + blk * block_elems,"),
 }
 
 
