@@ -591,6 +591,18 @@ def secondary_measurements(torch, pk, device, main_step):
     res["gather_blocks_512"] = {"ms": ms, "GB/s": 2 * 512 * blk_bytes / ms / 1e6}
     del gk, gv
 
+    # chained block hashes of the decode batch's token ids (prefix-cache lookup)
+    ctx = main_step.ctx
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)).to(device)
+    tok = torch.from_numpy(W.rng_for(3, 600).integers(0, 151936, int(ctx.sum()))
+                           .astype(np.int32)).to(device)
+    mb = int(ctx.max()) // 256
+    hashes = torch.empty((len(ctx), mb), dtype=torch.int64, device=device)
+    ms = timed(lambda: pk.block_hashes(tok, cu, 256, mb, out=hashes))
+    nfull = int((ctx // 256).sum())
+    res["block_hashes_qwen3_8b_batch"] = {"ms": ms, "full_blocks": nfull,
+                                          "GB/s": nfull * 256 * 4 / ms / 1e6}
+
     # long-context split decode (one layer)
     try:
         layer = _decode_layer("long_splitk_decode", torch, device)

@@ -160,6 +160,23 @@ PKV_API int pkv_scatter_blocks(const uint16_t* in_k, const uint16_t* in_v, const
                                pkv_cache_desc cache, void* stream);
 
 /*
+ * Chained block hashes for prefix-cache lookup ["nano-vllm 深度分析报告", section "创新之处" and
+ * table "可复用的模式与技巧": each full block is content-addressed by an xxhash64 that includes the
+ * hash of the preceding blocks, which makes the position part of the identity].
+ * For sequence b (tokens token_ids[cu_seqlens[b] .. cu_seqlens[b+1])) and each of its full blocks
+ * i < len_b / block_size:
+ *   out[b * max_blocks + i] = XXH64(seed 0) of [8-byte little-endian out[b*max_blocks + i-1],
+ *                              omitted for i = 0] ++ [the block's token ids, 4-byte little-endian]
+ * Entries for i >= the number of full blocks are set to 0. A sequence with more than max_blocks
+ * full blocks has the rest ignored and raises PKV_DEVERR_CTX_CLAMPED.
+ *   token_ids   device, int32;  cu_seqlens  device, [num_seqs + 1] int32, non-decreasing
+ *   block_size  even, 2..256;   out  device, [num_seqs, max_blocks] uint64
+ */
+PKV_API int pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
+                             int32_t num_seqs, int32_t block_size, int32_t max_blocks,
+                             uint64_t* out, void* stream);
+
+/*
  * Paged decode without any device allocation by the caller (no counterpart in the source pages:
  * it exists for callers of this library that cannot allocate device memory).
  * Some callers cannot call cudaMalloc for the decode workspace: a process that has given all of

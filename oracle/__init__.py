@@ -71,6 +71,11 @@ class Oracle:
         lib.oracle_scatter_blocks.restype = ctypes.c_int32
         lib.oracle_scatter_blocks.argtypes = [_u16p, _u16p, _i32p, ctypes.c_int32, _u16p, _u16p,
                                               ctypes.c_int32, i64]
+        lib.oracle_xxh64.restype = ctypes.c_uint64
+        lib.oracle_xxh64.argtypes = [ctypes.c_char_p, ctypes.c_int64, ctypes.c_uint64]
+        lib.oracle_block_hashes.restype = ctypes.c_int32
+        lib.oracle_block_hashes.argtypes = [_i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64)]
         self.lib = lib
 
     def max_threads(self) -> int:
@@ -184,6 +189,22 @@ class Oracle:
                                              len(ids), _ptr(kc, _u16p), _ptr(vc, _u16p),
                                              kc.shape[0], int(np.prod(kc.shape[1:])))
         return kc, vc, int(bad)
+
+
+    # -- Chained block hashes -------------------------------------------------------------------
+    def xxh64(self, data: bytes, seed: int = 0) -> int:
+        return int(self.lib.oracle_xxh64(data, len(data), seed))
+
+    def block_hashes(self, token_ids, cu_seqlens, block_size: int, max_blocks: int):
+        """Return ([num_seqs, max_blocks] uint64 with unhashed entries 0, clamped count)."""
+        tok = _c(token_ids, np.int32)
+        cu = _c(cu_seqlens, np.int32)
+        B = len(cu) - 1
+        out = np.zeros((B, max_blocks), np.uint64)
+        n = self.lib.oracle_block_hashes(_ptr(tok, _i32p), _ptr(cu, _i32p), B, block_size,
+                                         max_blocks,
+                                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+        return out, int(n)
 
 
 _default: Optional[Oracle] = None

@@ -313,3 +313,113 @@ int32_t oracle_scatter_blocks(const uint16_t *in_k, const uint16_t *in_v, const 
   }
   return bad;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Chained block hashes for prefix caching ["nano-vllm 深度分析报告", section "创新之处" and table
+ * "可复用的模式与技巧": each full block is content-addressed by an xxhash64 that includes the hash
+ * of the blocks before it, so equal hashes mean equal token prefixes, not just equal blocks].
+ * Reading: block i of a sequence hashes the byte string
+ *     [8-byte little-endian hash of block i-1, omitted for block 0] ++ [its block_size token ids
+ *      as 4-byte little-endian integers]
+ * with XXH64, seed 0. Only full blocks are hashed.
+ *
+ * XXH64 below follows the published xxHash specification (64-bit variant): four 64-bit lanes
+ * over 32-byte stripes, lane merge, length, 8/4/1-byte tail steps, final avalanche.
+ * ------------------------------------------------------------------------------------------- */
+static const uint64_t XXP1 = 0x9E3779B185EBCA87ull, XXP2 = 0xC2B2AE3D27D4EB4Full,
+                      XXP3 = 0x165667B19E3779F9ull, XXP4 = 0x85EBCA77C2B2AE63ull,
+                      XXP5 = 0x27D4EB2F165667C5ull;
+
+static uint64_t rotl64(uint64_t x, int r) { return (x << r) | (x >> (64 - r)); }
+
+static uint64_t read_le64(const uint8_t *p) {
+  uint64_t v = 0;
+  for (int i = 7; i >= 0; --i) v = (v << 8) | p[i];
+  return v;
+}
+
+static uint32_t read_le32(const uint8_t *p) {
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+static uint64_t xx_round(uint64_t acc, uint64_t lane) {
+  acc += lane * XXP2;
+  acc = rotl64(acc, 31);
+  return acc * XXP1;
+}
+
+uint64_t oracle_xxh64(const uint8_t *data, int64_t len, uint64_t seed) {
+  const uint8_t *p = data;
+  const uint8_t *end = data + len;
+  uint64_t acc;
+  if (len >= 32) {
+    uint64_t v1 = seed + XXP1 + XXP2, v2 = seed + XXP2, v3 = seed, v4 = seed - XXP1;
+    while (end - p >= 32) {
+      v1 = xx_round(v1, read_le64(p));
+      v2 = xx_round(v2, read_le64(p + 8));
+      v3 = xx_round(v3, read_le64(p + 16));
+      v4 = xx_round(v4, read_le64(p + 24));
+      p += 32;
+    }
+    acc = rotl64(v1, 1) + rotl64(v2, 7) + rotl64(v3, 12) + rotl64(v4, 18);
+    const uint64_t lanes[4] = {v1, v2, v3, v4};
+    for (int i = 0; i < 4; ++i) {
+      acc ^= xx_round(0, lanes[i]);
+      acc = acc * XXP1 + XXP4;
+    }
+  } else {
+    acc = seed + XXP5;
+  }
+  acc += (uint64_t)len;
+  while (end - p >= 8) {
+    acc ^= xx_round(0, read_le64(p));
+    acc = rotl64(acc, 27) * XXP1 + XXP4;
+    p += 8;
+  }
+  if (end - p >= 4) {
+    acc ^= (uint64_t)read_le32(p) * XXP1;
+    acc = rotl64(acc, 23) * XXP2 + XXP3;
+    p += 4;
+  }
+  while (p < end) {
+    acc ^= (uint64_t)(*p) * XXP5;
+    acc = rotl64(acc, 11) * XXP1;
+    ++p;
+  }
+  acc ^= acc >> 33;
+  acc *= XXP2;
+  acc ^= acc >> 29;
+  acc *= XXP3;
+  acc ^= acc >> 32;
+  return acc;
+}
+
+/* Hashes of the full blocks of each sequence: out[b * max_blocks + i] for i < len_b / block_size
+ * (tokens of sequence b are token_ids[cu_seqlens[b] .. cu_seqlens[b+1])). Returns the number of
+ * sequences with more full blocks than max_blocks (their extra blocks are not hashed). */
+int32_t oracle_block_hashes(const int32_t *token_ids, const int32_t *cu_seqlens, int32_t num_seqs,
+                            int32_t block_size, int32_t max_blocks, uint64_t *out) {
+  int32_t clamped = 0;
+  uint8_t *buf = (uint8_t *)malloc(8 + 4 * (size_t)block_size);
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t len = cu_seqlens[b + 1] - cu_seqlens[b];
+    int32_t nfull = len / block_size;
+    if (nfull > max_blocks) {
+      ++clamped;
+      nfull = max_blocks;
+    }
+    uint64_t parent = 0;
+    for (int32_t i = 0; i < nfull; ++i) {
+      size_t n = 0;
+      if (i > 0)
+        for (int k = 0; k < 8; ++k) buf[n++] = (uint8_t)(parent >> (8 * k));
+      const int32_t *tok = token_ids + cu_seqlens[b] + (int64_t)i * block_size;
+      for (int32_t t = 0; t < block_size; ++t)
+        for (int k = 0; k < 4; ++k) buf[n++] = (uint8_t)((uint32_t)tok[t] >> (8 * k));
+      parent = oracle_xxh64(buf, (int64_t)n, 0);
+      out[(int64_t)b * max_blocks + i] = parent;
+    }
+  }
+  free(buf);
+  return clamped;
+}

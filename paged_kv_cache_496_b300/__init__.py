@@ -79,6 +79,8 @@ def _load():
     L.pkv_gather_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, vp, vp, vp]
     L.pkv_scatter_blocks.restype = ctypes.c_int
     L.pkv_scatter_blocks.argtypes = [vp, vp, vp, i32, vp, vp, CacheDesc, vp]
+    L.pkv_block_hashes.restype = ctypes.c_int
+    L.pkv_block_hashes.argtypes = [vp, vp, i32, i32, i32, vp, vp]
     L.pkv_selftest_bounded_wait.restype = ctypes.c_int
     L.pkv_selftest_bounded_wait.argtypes = [vp]
     L.pkv_get_device_error.restype = ctypes.c_int
@@ -287,3 +289,17 @@ def scatter_blocks(in_k, in_v, ids, k_cache, v_cache, stream=None):
     _check(lib.pkv_scatter_blocks(in_k.data_ptr(), in_v.data_ptr(), ids.data_ptr(),
                                   ids.shape[0], k_cache.data_ptr(), v_cache.data_ptr(),
                                   _cache_desc(k_cache), _stream_ptr(stream)))
+
+
+def block_hashes(token_ids, cu_seqlens, block_size: int, max_blocks: int, out=None, stream=None):
+    """Chained xxhash64 of each sequence's full blocks: int64 tensor [num_seqs, max_blocks]
+    holding the uint64 hash bits (0 where a sequence has no full block)."""
+    _need(token_ids, "token_ids", torch.int32, 1)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    B = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty((B, max_blocks), dtype=torch.int64, device=token_ids.device)
+    _need(out, "out", torch.int64, 2)
+    _check(lib.pkv_block_hashes(token_ids.data_ptr(), cu_seqlens.data_ptr(), B, int(block_size),
+                                int(max_blocks), out.data_ptr(), _stream_ptr(stream)))
+    return out

@@ -259,6 +259,24 @@ int pkv_scatter_blocks(const uint16_t* in_k, const uint16_t* in_v, const int32_t
                     const_cast<uint16_t*>(in_v), stream);
 }
 
+int pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens, int32_t num_seqs,
+                     int32_t block_size, int32_t max_blocks, uint64_t* out, void* stream) {
+  g_last_error[0] = 0;
+  if (num_seqs < 0 || max_blocks < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs and max_blocks must be >= 0");
+  if (block_size < 2 || (block_size & 1) || block_size > 256)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (must be even, 2..256)", block_size);
+  if (num_seqs == 0 || max_blocks == 0) return PKV_OK;
+  if (!token_ids || !cu_seqlens || !out) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  DeviceInfo d;
+  int st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_block_hashes(token_ids, cu_seqlens, num_seqs, block_size, max_blocks,
+                                      out, d.flags, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block hash launch");
+  return PKV_OK;
+}
+
 int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
                          int32_t max_context_len, int32_t split_tokens_hint,
                          pkv_decode_plan* plan) {

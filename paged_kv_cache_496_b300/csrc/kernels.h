@@ -55,6 +55,11 @@ cudaError_t launch_block_move(int mode, uint16_t* k_cache, uint16_t* v_cache,
                               uint16_t* buf_k, uint16_t* buf_v, int num_sms, int* flags,
                               cudaStream_t stream);
 
+// Chained xxhash64 of every full block of each sequence (one thread per sequence).
+cudaError_t launch_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int32_t block_size, int32_t max_blocks,
+                                uint64_t* out, int* flags, cudaStream_t stream);
+
 // Rows of the K/V TMA box the decode kernel expects (tile tokens, or the block size if smaller).
 int decode_box_rows(int head_dim, int group, int block_size);
 

@@ -415,6 +415,52 @@ def pin_block_moves_match_numpy(orc):
     assert np.array_equal(back, kc[ids])
 
 
+# ------------------------------------------------------------------------------------------------
+# Chained block hashes (prefix caching)
+# ------------------------------------------------------------------------------------------------
+
+
+def pin_xxh64_published_vectors(orc):
+    with open(os.path.join(GOLDEN, "xxh64_vectors.json")) as f:
+        g = json.load(f)
+    for v in g["vectors"]:
+        got = orc.xxh64(v["input"].encode(), v["seed"])
+        assert got == int(v["xxh64"], 16), f"XXH64({v['input']!r}) = {got:016x}"
+
+
+def pin_block_hash_chain(orc):
+    import struct
+    rng = W.rng_for(42, 0)
+    BS = 16
+    toks = rng.integers(0, 151936, size=5 * BS + 7, dtype=np.int64).astype(np.int32)
+    out, clamped = orc.block_hashes(toks, np.array([0, len(toks)], np.int32), BS, 8)
+    assert clamped == 0 and np.all(out[0, 5:] == 0), "only the 5 full blocks are hashed"
+    parent = None
+    for i in range(5):
+        blk = struct.pack("<%di" % BS, *toks[i * BS:(i + 1) * BS].tolist())
+        data = (b"" if parent is None else struct.pack("<Q", parent)) + blk
+        parent = orc.xxh64(data, 0)
+        assert int(out[0, i]) == parent, f"block {i}: chain or byte layout differs"
+
+
+def pin_block_hash_prefix_semantics(orc):
+    rng = W.rng_for(43, 0)
+    BS = 16
+    shared = rng.integers(0, 1000, size=3 * BS, dtype=np.int64).astype(np.int32)
+    a = np.concatenate([shared, rng.integers(0, 1000, size=2 * BS).astype(np.int32)])
+    b = np.concatenate([shared, rng.integers(0, 1000, size=2 * BS).astype(np.int32)])
+    same = np.tile(shared[:BS], 2)  # the same block content at positions 0 and 1
+    toks = np.concatenate([a, b, same]).astype(np.int32)
+    cu = np.array([0, len(a), len(a) + len(b), len(toks)], np.int32)
+    out, _ = orc.block_hashes(toks, cu, BS, 5)
+    assert np.array_equal(out[0, :3], out[1, :3]), "a shared prefix must hash identically"
+    assert np.all(out[0, 3:5] != out[1, 3:5]), "different continuations must differ"
+    assert out[2, 0] != out[2, 1], "equal blocks at different positions must differ"
+    assert out[2, 0] == out[0, 0], "block 0 depends only on its own tokens"
+    _, clamped = orc.block_hashes(toks, cu, BS, 2)
+    assert clamped == 2  # a and b have 5 full blocks; the third has exactly 2
+
+
 ALL_PINS = [
     pin_store_matches_numpy_scatter,
     pin_store_padding_and_invalid,
@@ -432,4 +478,7 @@ ALL_PINS = [
     pin_prefill_row_equals_decode,
     pin_prefill_shared_vs_duplicated_prefix,
     pin_block_moves_match_numpy,
+    pin_xxh64_published_vectors,
+    pin_block_hash_chain,
+    pin_block_hash_prefix_semantics,
 ]

@@ -30,6 +30,14 @@ MUTANTS = {
     "prefix_keys_from_new_rows": ("bad |= oracle_gather_head(k_cache, num_blocks, block_size, num_kv_heads, head_dim, bt_row,\n                                P, g, K);",
                                   "bad |= oracle_gather_head(v_cache, num_blocks, block_size, num_kv_heads, head_dim, bt_row,\n                                P, g, K);"),
     "max_not_tracked": ("if (s[j] > m) m = s[j];", "if (s[j] < m) m = s[j];"),
+    "xxh64_wrong_round_rotation": ("  acc = rotl64(acc, 31);\n  return acc * XXP1;",
+                                   "  acc = rotl64(acc, 33);\n  return acc * XXP1;"),
+    "xxh64_tail8_rotation": ("acc = rotl64(acc, 27) * XXP1 + XXP4;",
+                             "acc = rotl64(acc, 29) * XXP1 + XXP4;"),
+    "chain_parent_big_endian": ("buf[n++] = (uint8_t)(parent >> (8 * k));",
+                                "buf[n++] = (uint8_t)(parent >> (56 - 8 * k));"),
+    "chain_hashes_partial_block": ("int32_t nfull = len / block_size;",
+                                   "int32_t nfull = (len + block_size - 1) / block_size;"),
     "cow_copies_backwards": ("memcpy(k_cache + dst * block_elems, k_cache + src * block_elems,",
                              "memcpy(k_cache + src * block_elems, k_cache + dst * block_elems,"),
     "gather_reads_v_for_k": ("memcpy(out_k + i * block_elems, k_cache + blk * block_elems,",
