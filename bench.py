@@ -147,7 +147,8 @@ def job_throughput(units_per_rank, seconds_max, world):
 class DecodeStep:
     """All layers of one decode step, resident in HBM."""
 
-    def __init__(self, name, torch, pk, device, log_fill=True, num_seqs=None, num_layers=None):
+    def __init__(self, name, torch, pk, device, log_fill=True, num_seqs=None, num_layers=None,
+                 fused=False):
         self.w = w = W.WORKLOADS[name]
         self.torch, self.pk = torch, pk
         self.ctx = W.decode_lengths(name)
@@ -188,19 +189,34 @@ class DecodeStep:
         self.ws = torch.empty(max(256, self.plan.workspace_bytes), dtype=torch.uint8,
                               device=device)
         self.kv_bytes_per_layer = int(self.ctx.sum()) * w.kv_bytes_per_token
-        self.launches_per_step = 3 * self.L  # store, decode plan, decode
+        self.fused = fused
+        # per layer: (store,) decode plan, decode
+        self.launches_per_step = (2 if fused else 3) * self.L
 
-    def run(self, events=None):
+    def layer(self, l, pre=None, post=None):
+        """Store the newest token of every sequence and decode layer l."""
         pk = self.pk
-        for l in range(self.L):
-            kc, vc = self.pools[l % self.n_pools]
+        kc, vc = self.pools[l % self.n_pools]
+        if not self.fused:
             pk.kv_store(self.k_new[l], self.v_new[l], self.slots_dev, kc, vc)
-            if events is not None:
-                events[l][0].record()
+        if pre is not None:
+            pre.record()
+        if self.fused:
+            pk.paged_decode_store(self.q[l], self.k_new[l], self.v_new[l], self.slots_dev, kc, vc,
+                                  self.bt_dev, self.ctx_dev, self.scale, out=self.out[l],
+                                  plan=self.plan, workspace=self.ws)
+        else:
             pk.paged_decode(self.q[l], kc, vc, self.bt_dev, self.ctx_dev, self.scale,
                             out=self.out[l], plan=self.plan, workspace=self.ws)
-            if events is not None:
-                events[l][1].record()
+        if post is not None:
+            post.record()
+
+    def run(self, events=None):
+        for l in range(self.L):
+            if events is None:
+                self.layer(l)
+            else:
+                self.layer(l, events[l][0], events[l][1])
 
 
 class PrefillStep:
@@ -371,6 +387,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--fused", action="store_true",
+                    help="one pkv_paged_decode_store per layer instead of pkv_kv_store then "
+                         "pkv_paged_decode")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload (not a bench number)")
     ap.add_argument("--num-seqs", type=int, default=0,
@@ -399,7 +418,7 @@ def main():
     if args.workload == "prefix_prefill":
         return prefill_arm(args, torch, pk, device)
     step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
-                      num_layers=args.layers)
+                      num_layers=args.layers, fused=args.fused)
     reduced = bool(args.num_seqs or args.layers)
     w = step.w
 
@@ -475,10 +494,7 @@ def main():
                     ev_in[l].record(s_in)
             for l in range(step.L):
                 main.wait_event(ev_in[l])
-                kc, vc = step.pools[l % step.n_pools]
-                pk.kv_store(step.k_new[l], step.v_new[l], step.slots_dev, kc, vc)
-                pk.paged_decode(step.q[l], kc, vc, step.bt_dev, step.ctx_dev, step.scale,
-                                out=step.out[l], plan=step.plan, workspace=step.ws)
+                step.layer(l)
                 ev_done[l].record(main)
                 s_out.wait_event(ev_done[l])
                 with torch.cuda.stream(s_out):
@@ -527,12 +543,15 @@ def main():
                        "mean_context": float(step.ctx.mean()),
                        "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
                        "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
-                       "step": "per layer: kv_store (1 token/seq) + paged_decode",
+                       "step": ("per layer: kv_store (1 token/seq) fused into paged_decode"
+                                if step.fused else
+                                "per layer: kv_store (1 token/seq), then paged_decode"),
                        "parallelism": f"replicas x{world}",
                        "reduced_for_profiling": reduced},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "paged_decode (plan + persistent decode kernel)",
+                         "kernel": "paged_decode (plan + persistent decode kernel%s)"
+                                   % (", store fused" if step.fused else ""),
                          "algorithmic_bytes_per_launch": step.kv_bytes_per_layer,
                          "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind},
             "clocks": clocks.summary(),
@@ -564,6 +583,14 @@ def secondary_measurements(torch, pk, device, main_step):
         b.record()
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
+
+    # the same step through the other API: the store fused into the decode kernel, or not
+    was = main_step.fused
+    main_step.fused = not was
+    ms = timed(main_step.run, reps=3)
+    main_step.fused = was
+    res["fused_step" if not was else "unfused_step"] = {
+        "ms": ms, "GB/s": main_step.kv_bytes_per_layer * main_step.L / ms / 1e6}
 
     # kv_store alone at the decode size (launch-bound) and at the prefill size (bandwidth-bound)
     kc, vc = main_step.pools[0]

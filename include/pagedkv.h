@@ -207,6 +207,29 @@ PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cach
                                        void* stream);
 
 /*
+ * Decode step with the KV store fused in ["nano-vllm 深度分析报告", table "可复用的模式与技巧":
+ * the store of the step's new tokens precedes attention; fusing the two removes one launch].
+ * Equivalent to pkv_kv_store(k_new, v_new, slot_mapping, num_seqs, ...) followed by
+ * pkv_paged_decode(...) when, as in a decode step, slot_mapping[b] is the slot of position
+ * context_lens[b] - 1 of sequence b (or -1 for a padded entry with context 0):
+ *   - attention for sequence b reads positions 0 .. ctx-2 from the cache and position ctx-1 from
+ *     k_new[b] / v_new[b] (so it never waits for the cache write);
+ *   - k_new[b], v_new[b] are written to slot_mapping[b] (skipped when -1). A slot that is not the
+ *     block table's slot of position ctx-1 is still written and raises PKV_DEVERR_BAD_SLOT.
+ *   k_new, v_new  device, [num_seqs, num_kv_heads, head_dim] bf16 (one new token per sequence)
+ *   slot_mapping  device, [num_seqs] int32
+ * Other arguments as pkv_paged_decode; k_cache and v_cache are written.
+ */
+PKV_API int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                   const int32_t* slot_mapping, uint16_t* k_cache,
+                                   uint16_t* v_cache, pkv_cache_desc cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+                                   uint16_t* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
  * Varlen causal paged prefill [P1 PagedAttention; P3 prefix-cache hits share blocks].
  * Sequence b has q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens (rows cu_seqlens_q[b] ..
  * of q, k, v) and k_len = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys. The first P = k_len - q_len

@@ -70,6 +70,9 @@ def _load():
     L.pkv_paged_decode.restype = ctypes.c_int
     L.pkv_paged_decode.argtypes = [vp, vp, vp, CacheDesc, vp, i32, vp, i32, i32, f32,
                                    ctypes.POINTER(DecodePlan), vp, vp, sz, vp]
+    L.pkv_paged_decode_store.restype = ctypes.c_int
+    L.pkv_paged_decode_store.argtypes = [vp, vp, vp, vp, vp, vp, CacheDesc, vp, i32, vp, i32,
+                                         i32, f32, ctypes.POINTER(DecodePlan), vp, vp, sz, vp]
     L.pkv_paged_prefill.restype = ctypes.c_int
     L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp,
                                     CacheDesc, i32, f32, vp, vp]
@@ -202,6 +205,42 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
                                 block_tables.shape[1], context_lens.data_ptr(), B, Hq,
                                 float(scale), ctypes.byref(plan), out.data_ptr(),
                                 workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+    return out
+
+
+def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                       context_lens, scale: float, out=None, max_context_len: Optional[int] = None,
+                       split_tokens: int = 0, plan: Optional[DecodePlan] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None):
+    """One decode step with the store fused in: writes k_new[b], v_new[b] to slot_mapping[b] and
+    attends over context_lens[b] tokens, the last of which is taken from k_new / v_new."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    if (k_new.shape != (B,) + tuple(k_cache.shape[2:]) or v_new.shape != k_new.shape
+            or slot_mapping.shape[0] != B):
+        raise ValueError("k_new / v_new must be [num_seqs, Hkv, D] and slot_mapping [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    if plan is None:
+        if max_context_len is None:
+            max_context_len = int(context_lens.max().item()) if B else 0
+        plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens)
+    if workspace is None:
+        workspace = workspace_for(plan, q.device)
+    _check(lib.pkv_paged_decode_store(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                      slot_mapping.data_ptr(), k_cache.data_ptr(),
+                                      v_cache.data_ptr(), _cache_desc(k_cache),
+                                      block_tables.data_ptr(), block_tables.shape[1],
+                                      context_lens.data_ptr(), B, Hq, float(scale),
+                                      ctypes.byref(plan), out.data_ptr(), workspace.data_ptr(),
+                                      workspace.numel(), _stream_ptr(stream)))
     return out
 
 

@@ -312,11 +312,13 @@ int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c
   return PKV_OK;
 }
 
-int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                     pkv_cache_desc cache, const int32_t* block_tables,
-                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
-                     int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
-                     uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                       pkv_cache_desc cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                       int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+                       uint16_t* out, void* workspace, size_t workspace_bytes, void* stream,
+                       const uint16_t* k_new, const uint16_t* v_new,
+                       const int32_t* slot_mapping) {
   g_last_error[0] = 0;
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
@@ -372,10 +374,40 @@ int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
   a.auto_split = plan->auto_split != 0;
   a.out = out;
   a.flags = d.flags;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
   cudaError_t e = launch_paged_decode(a, tk, tv, d.num_sms, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return fail(PKV_ERR_UNSUPPORTED, "no decode instance");
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;
+}
+
+int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     pkv_cache_desc cache, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                     int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
+                     uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                     num_seqs, num_q_heads, scale, plan, out, workspace, workspace_bytes, stream,
+                     nullptr, nullptr, nullptr);
+}
+
+int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                           const int32_t* slot_mapping, uint16_t* k_cache, uint16_t* v_cache,
+                           pkv_cache_desc cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t num_q_heads, float scale,
+                           const pkv_decode_plan* plan, uint16_t* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (num_seqs > 0 && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  return decode_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                     num_seqs, num_q_heads, scale, plan, out, workspace, workspace_bytes, stream,
+                     k_new, v_new, slot_mapping);
 }
 
 int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -46,6 +46,10 @@ struct DecodeArgs {
   uint16_t* out;
   DecodeWorkspace ws;
   int* flags;
+  // fused store (all null for a plain decode): newest token of sequence b, [B, Hkv, D]
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
+  const int32_t* slot_mapping = nullptr;
 };
 
 // Whole-block moves: mode 0 copies (src, dst) pairs inside the caches, mode 1 gathers blocks

@@ -62,6 +62,15 @@ struct DecodeParams {
   int32_t max_splits;
   int32_t cap_tokens;  // contexts are clamped to this many tokens (table and plan capacity)
   float qk_scale_log2;
+  // Fused store (NEXT step of a decode): the newest token of sequence b comes from k_new[b] /
+  // v_new[b] ([B, Hkv, D]) instead of the cache, and is written to slot_mapping[b].
+  int32_t fuse_store;
+  int32_t num_kv_heads;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
 };
 
 template <int D, int GH>
@@ -443,6 +452,14 @@ __global__ void __maxnreg__(168)
   for (int r = 0; r < VPL; ++r) l_lane[r] = 0.f;
   uint32_t use = 0;
   uint32_t item = 0;
+  // fused store: this warp owns the newest token's row in the item's last tile
+  int fuse_row = -1;   // row of the newest token in the last tile (this warp's), or -1
+  int fuse_g = 0;      // its kv head
+  int fuse_pos = 0;    // its position in the sequence
+  int fuse_slot = -1;  // where it goes in the cache (-1: this CTA does not write it)
+  int fuse_blk = 0;    // block table entry of fuse_pos, to check the slot against
+  uint4 fuse_val = make_uint4(0u, 0u, 0u, 0u);
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks of one (token, kv head) row
 
   while (true) {
     const int st = use % T::kStages;
@@ -494,6 +511,50 @@ __global__ void __maxnreg__(168)
         }
       }
       __syncwarp();
+      // Fused store: the loads are issued now and used only at the item's last tile.
+      fuse_row = -1;
+      if (p.fuse_store && meta[st].split == meta[st].nsplit - 1) {
+        const int b = meta[st].b, x = meta[st].x;
+        const int pos = meta[st].tok_end - 1;  // the last chunk ends at the context length
+        const int r = pos % T::kTileT;
+        if (r / T::kTokPerWarp == warp) {
+          fuse_row = r;
+          fuse_pos = pos;
+          fuse_g = x / p.groups_per_kv;
+          if (lane < 2 * kRowChunks) {
+            const uint16_t* src = (lane < kRowChunks ? p.k_new : p.v_new) +
+                                  ((int64_t)b * p.num_kv_heads + fuse_g) * D +
+                                  (lane % kRowChunks) * 8;
+            fuse_val = __ldg(reinterpret_cast<const uint4*>(src));
+          }
+          fuse_slot = -1;
+          if (x % p.groups_per_kv == 0) {  // one head group per kv head writes the cache
+            fuse_slot = __ldg(p.slot_mapping + b);
+            fuse_blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks + pos / p.block_size);
+          }
+        }
+      }
+    }
+
+    if (fuse_row >= 0 && (mflags & kMetaLast)) {
+      // put the newest token into the landed tile (the cache copy may not be written yet)
+      const bool writes = fuse_slot >= 0 && fuse_slot < p.num_blocks * p.block_size;
+      if (lane < 2 * kRowChunks) {
+        uint8_t* dst = tiles + st * T::kStageBytes + (lane < kRowChunks ? 0 : T::kTileBytes) +
+                       fuse_row * T::kRowBytes + (lane % kRowChunks) * 16;
+        *reinterpret_cast<uint4*>(dst) = fuse_val;
+        if (writes)
+          *reinterpret_cast<uint4*>((lane < kRowChunks ? p.k_cache : p.v_cache) +
+                                    ((int64_t)fuse_slot * p.num_kv_heads + fuse_g) * D +
+                                    (lane % kRowChunks) * 8) = fuse_val;
+      }
+      if (lane == 0 && fuse_slot != -1) {
+        const int expect = fuse_blk * p.block_size + fuse_pos % p.block_size;
+        if (!writes || fuse_slot != expect) raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
+      }
+      fence_async_shared_cta();  // the stage will be refilled by TMA later
+      __syncwarp();
+      fuse_row = -1;
     }
 
     if (!(mflags & kMetaZero)) {
@@ -798,6 +859,13 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   if (cap > 0x7fffffff) cap = 0x7fffffff;
   p.cap_tokens = (int32_t)cap;
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
+  p.fuse_store = a.k_new != nullptr ? 1 : 0;
+  p.num_kv_heads = a.cache.num_kv_heads;
+  p.k_new = a.k_new;
+  p.v_new = a.v_new;
+  p.slot_mapping = a.slot_mapping;
+  p.k_cache = const_cast<uint16_t*>(a.k_cache);
+  p.v_cache = const_cast<uint16_t*>(a.v_cache);
 
   const int64_t upper = (int64_t)a.num_seqs * a.max_splits * p.head_groups;
   int64_t grid = (int64_t)num_sms * ctas_per_sm;
