@@ -312,7 +312,9 @@ __global__ void __maxnreg__(168)
     const int ent_per_tile = (T::kTileT + bs - 1) / bs;
     uint32_t issue = 0;
     bool ok = true;
-    int win_b = -1, win_base = 0, win_val = -1;
+    // Block-table window: entries [win_base, win_base + 32) of sequence win_b, one per lane, and
+    // the next 32 entries prefetched so that walking on does not stall the pipeline.
+    int win_b = -1, win_base = 0, win_val = -1, nxt_val = -1;
 
     auto claim = [&]() -> uint32_t {
       uint32_t c = 0;
@@ -370,10 +372,17 @@ __global__ void __maxnreg__(168)
         const int st = issue % T::kStages;
         const int e0 = tok0 / bs;
         if (win_b != b || e0 < win_base || e0 + ent_per_tile > win_base + 32) {
-          win_b = b;
-          win_base = e0;
-          const int e = e0 + lane;
-          win_val = e < need_ent ? __ldg(bt_row + e) : -1;
+          if (win_b == b && e0 >= win_base + 32 && e0 + ent_per_tile <= win_base + 64) {
+            win_base += 32;  // step into the prefetched window
+            win_val = nxt_val;
+          } else {
+            win_b = b;
+            win_base = e0;
+            const int e = e0 + lane;
+            win_val = e < need_ent ? __ldg(bt_row + e) : -1;
+          }
+          const int e = win_base + 32 + lane;
+          nxt_val = e < need_ent ? __ldg(bt_row + e) : -1;
         }
         int rows[T::kMaxSub];
         uint32_t bytes = 0;
@@ -787,19 +796,36 @@ __global__ void __maxnreg__(168)
           const int h = o / D, d = o % D;
           const int head = mt.x * GH + h;
           const int64_t base = (int64_t)mt.b * p.max_splits * p.num_q_heads + head;
-          float M = -INFINITY;
-          for (int sp = 0; sp < mt.nsplit; ++sp)
-            M = fmaxf(M, __ldcg(p.part_ml + (base + (int64_t)sp * p.num_q_heads) * (D / 64) +
-                                d / 64).x);
-          float den = 0.f, n0 = 0.f, n1 = 0.f;
-          for (int sp = 0; sp < mt.nsplit; ++sp) {
-            const int64_t pi = base + (int64_t)sp * p.num_q_heads;
-            const float2 ml = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
-            const float wt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-            den += wt * ml.y;
-            const float2 a = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
-            n0 += wt * a.x;
-            n1 += wt * a.y;
+          // one pass with a running max, eight chunks' loads in flight at a time
+          float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
+          for (int sp0 = 0; sp0 < mt.nsplit; sp0 += 8) {
+            float2 ml[8], a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              ml[u] = make_float2(-INFINITY, 0.f);
+              a[u] = make_float2(0.f, 0.f);
+              if (sp0 + u < mt.nsplit) {
+                const int64_t pi = base + (int64_t)(sp0 + u) * p.num_q_heads;
+                ml[u] = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
+                a[u] = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
+              }
+            }
+            float mnew = M;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mnew = fmaxf(mnew, ml[u].x);
+            if (mnew == -INFINITY) continue;
+            const float keep = M == -INFINITY ? 0.f : fast_exp2(M - mnew);
+            den *= keep;
+            n0 *= keep;
+            n1 *= keep;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float wt = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mnew);
+              den += wt * ml[u].y;
+              n0 += wt * a[u].x;
+              n1 += wt * a[u].y;
+            }
+            M = mnew;
           }
           const float inv = den > 0.f ? 1.f / den : 0.f;
           *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)mt.b * p.num_q_heads + head) *
