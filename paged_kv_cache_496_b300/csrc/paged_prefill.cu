@@ -10,7 +10,9 @@
 //  * The 128 rows are 128/G positions x the G query heads that share the kv head, so each K/V
 //    tile feeds all of them (rows ordered position-major, as the Q TMA box delivers them).
 //  * Warp 0 loads Q once and streams 64-key K and V tiles through the block table with 3-D TMA
-//    boxes in 128-byte swizzle (the layout the tensor core reads), two stages deep.
+//    boxes in 128-byte swizzle (the layout the tensor core reads). K and V have their own
+//    two-deep rings and barriers, and K runs one tile ahead of V: a K buffer is free as soon as
+//    its S = Q K^T is done, so the next K is in flight while the softmax of the current tile runs.
 //  * Warp 1 allocates 256 TMEM columns and, from one thread, issues S = Q K^T (M=128, N=64,
 //    K=128: eight kind::f16 MMAs, K-major operands) into TMEM columns [0, 64) and O += P V
 //    (M=128, N=128, K=64: four MMAs, V read MN-major) into columns [64, 192).
@@ -48,9 +50,11 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
 constexpr int kOffP = kOffKV + kNStage * kStage;
 constexpr int kOffBar = kOffP + kPBytes;
-// barriers: q, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done, mma_done
-constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarSFull = 5, kBarSFree = 6,
-              kBarPFull = 7, kBarODone = 8, kBarMma = 9, kNumBars = 10;
+// barriers: q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, o_done,
+// mma_done
+constexpr int kBarQ = 0, kBarFullK = 1, kBarEmptyK = 3, kBarFullV = 5, kBarEmptyV = 7,
+              kBarSFull = 9, kBarSFree = 10, kBarPFull = 11, kBarODone = 12, kBarMma = 13,
+              kNumBars = 14;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmemSlot + 16;
 static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -121,8 +125,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kNStage; ++s) {
-      mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarFullK + s), 1);
+      mbar_init(bar(kBarEmptyK + s), 1);
+      mbar_init(bar(kBarFullV + s), 1);
+      mbar_init(bar(kBarEmptyV + s), 1);
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFree), 4);
@@ -166,72 +172,95 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       bt_row = p.block_tables + (int64_t)b * p.max_blocks;
     }
     int win_base = -1000000, win_val = -1;
-    int issued = 0;
-    for (int j = 0; j < n_kt && ok; ++j) {
-      const int st = j & 1;
-      const int key0 = j * kKeys;
+    int issued_k = 0, issued_v = 0;
+    int prev_rows[kKeys / 16];
+    // Issue order K0, K1, V0, K2, V1, ...: step j loads K(j) (if j < n_kt), then V(j-1).
+    for (int j = 0; j <= n_kt && ok; ++j) {
       int rows[kKeys / 16];
 #pragma unroll
       for (int sb = 0; sb < kKeys / 16; ++sb) rows[sb] = p.oob_row;
-      if (paged) {
-        const int e0 = key0 / bs;
-        const int ent = (kKeys + bs - 1) / bs;
-        if (e0 < win_base || e0 + ent > win_base + 32) {
-          win_base = e0;
-          const int e = e0 + lane;
-          win_val = e < need_ent ? __ldg(bt_row + e) : -1;
-        }
-#pragma unroll
-        for (int sb = 0; sb < kKeys / 16; ++sb) {
-          if (sb < nsub) {
-            const int key = key0 + sb * box;
-            const int blk = __shfl_sync(kFullMask, win_val, (key / bs - win_base) & 31);
-            if (key < k_len && key / bs < need_ent) {
-              if (blk >= 0 && blk < p.num_blocks) {
-                rows[sb] = blk * bs + (key & (bs - 1));
-              } else if (lane == 0) {
-                raise_flag(p.flags, PKV_DEVERR_BAD_BLOCK);
-              }
-            }
+      const int key0 = j * kKeys;
+      if (j < n_kt) {
+        if (paged) {
+          const int e0 = key0 / bs;
+          const int ent = (kKeys + bs - 1) / bs;
+          if (e0 < win_base || e0 + ent > win_base + 32) {
+            win_base = e0;
+            const int e = e0 + lane;
+            win_val = e < need_ent ? __ldg(bt_row + e) : -1;
           }
-        }
-      } else {
-#pragma unroll
-        for (int sb = 0; sb < kKeys / 16; ++sb)
-          if (sb < nsub) rows[sb] = q_start + key0 + sb * box;
-      }
-      if (lane == 0) {
-        ok = mbar_wait(bar(kBarEmpty + st), ((j >> 1) & 1) ^ 1);
-        if (ok) {
-          const uint32_t full = bar(kBarFull + st);
-          mbar_arrive_expect_tx(full, kStage);
-          const uint32_t kd = sbase + kOffKV + st * kStage;
-          const uint32_t vd = kd + kKTile;
 #pragma unroll
           for (int sb = 0; sb < kKeys / 16; ++sb) {
             if (sb < nsub) {
-              const uint32_t off = (uint32_t)(sb * box * 128);
-              tma_load_3d(kd + off, &tmap_k, 0, g, rows[sb], full);
-              tma_load_3d(kd + kKHalf + off, &tmap_k, 64, g, rows[sb], full);
-              tma_load_3d(vd + off, &tmap_v, 0, g, rows[sb], full);
-              tma_load_3d(vd + kKHalf + off, &tmap_v, 64, g, rows[sb], full);
+              const int key = key0 + sb * box;
+              const int blk = __shfl_sync(kFullMask, win_val, (key / bs - win_base) & 31);
+              if (key < k_len && key / bs < need_ent) {
+                if (blk >= 0 && blk < p.num_blocks) {
+                  rows[sb] = blk * bs + (key & (bs - 1));
+                } else if (lane == 0) {
+                  raise_flag(p.flags, PKV_DEVERR_BAD_BLOCK);
+                }
+              }
             }
           }
-          ++issued;
         } else {
-          raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+#pragma unroll
+          for (int sb = 0; sb < kKeys / 16; ++sb)
+            if (sb < nsub) rows[sb] = q_start + key0 + sb * box;
         }
       }
+      if (lane == 0) {
+        if (j < n_kt) {
+          const int st = j & 1;
+          ok = mbar_wait(bar(kBarEmptyK + st), ((j >> 1) & 1) ^ 1);
+          if (ok) {
+            const uint32_t full = bar(kBarFullK + st);
+            mbar_arrive_expect_tx(full, kKTile);
+            const uint32_t kd = sbase + kOffKV + st * kStage;
+#pragma unroll
+            for (int sb = 0; sb < kKeys / 16; ++sb) {
+              if (sb < nsub) {
+                const uint32_t off = (uint32_t)(sb * box * 128);
+                tma_load_3d(kd + off, &tmap_k, 0, g, rows[sb], full);
+                tma_load_3d(kd + kKHalf + off, &tmap_k, 64, g, rows[sb], full);
+              }
+            }
+            ++issued_k;
+          }
+        }
+        if (ok && j > 0) {
+          const int jv = j - 1, st = jv & 1;
+          ok = mbar_wait(bar(kBarEmptyV + st), ((jv >> 1) & 1) ^ 1);
+          if (ok) {
+            const uint32_t full = bar(kBarFullV + st);
+            mbar_arrive_expect_tx(full, kKTile);
+            const uint32_t vd = sbase + kOffKV + st * kStage + kKTile;
+#pragma unroll
+            for (int sb = 0; sb < kKeys / 16; ++sb) {
+              if (sb < nsub) {
+                const uint32_t off = (uint32_t)(sb * box * 128);
+                tma_load_3d(vd + off, &tmap_v, 0, g, prev_rows[sb], full);
+                tma_load_3d(vd + kKHalf + off, &tmap_v, 64, g, prev_rows[sb], full);
+              }
+            }
+            ++issued_v;
+          }
+        }
+        if (!ok) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+      }
+#pragma unroll
+      for (int sb = 0; sb < kKeys / 16; ++sb) prev_rows[sb] = rows[sb];
       ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0) {
       // never leave while a copy into this CTA's shared memory may be in flight
       if (!mbar_wait(bar(kBarQ), 0)) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
-      for (int i = (issued > kNStage ? issued - kNStage : 0); i < issued; ++i)
-        if (!mbar_wait(bar(kBarFull + (i & 1)), (i >> 1) & 1)) {
-          raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
-          break;
-        }
+      bool drained = true;
+      for (int i = (issued_k > kNStage ? issued_k - kNStage : 0); i < issued_k && drained; ++i)
+        drained = mbar_wait(bar(kBarFullK + (i & 1)), (i >> 1) & 1);
+      for (int i = (issued_v > kNStage ? issued_v - kNStage : 0); i < issued_v && drained; ++i)
+        drained = mbar_wait(bar(kBarFullV + (i & 1)), (i >> 1) & 1);
+      if (!drained) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ============================ MMA issuer (one thread) ============================
@@ -241,7 +270,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       bool ok = mbar_wait(bar(kBarQ), 0);
       auto issue_pv = [&](int jj) {
         if (!ok) return;
-        ok = mbar_wait(bar(kBarPFull), jj & 1);
+        ok = mbar_wait(bar(kBarFullV + (jj & 1)), (jj >> 1) & 1);
+        if (ok) ok = mbar_wait(bar(kBarPFull), jj & 1);
         if (!ok) return;
         tc_fence_after_sync();
         const uint32_t vbase = sbase + kOffKV + (jj & 1) * kStage + kKTile;
@@ -252,11 +282,11 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           tc_mma_f16(tmem + kColO, a, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kBarODone));
-        tc_commit(bar(kBarEmpty + (jj & 1)));
+        tc_commit(bar(kBarEmptyV + (jj & 1)));
       };
       for (int j = 0; j < n_kt && ok; ++j) {
         const int st = j & 1;
-        ok = mbar_wait(bar(kBarFull + st), (j >> 1) & 1);
+        ok = mbar_wait(bar(kBarFullK + st), (j >> 1) & 1);
         if (ok && j > 0) ok = mbar_wait(bar(kBarSFree), (j - 1) & 1);
         if (!ok) break;
         tc_fence_after_sync();
@@ -269,6 +299,7 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           tc_mma_f16(tmem + kColS, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar(kBarSFull));
+        tc_commit(bar(kBarEmptyK + st));
         if (j > 0) issue_pv(j - 1);
       }
       if (ok) issue_pv(n_kt - 1);
@@ -384,7 +415,7 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       if (j == n_kt - 1 && kbase + kKeys > k_len) {
         // V rows past the last key hold whatever the cache holds there: zero them (after the
         // stage's copy has landed)
-        ok = mbar_wait(bar(kBarFull + (j & 1)), (j >> 1) & 1);
+        ok = mbar_wait(bar(kBarFullV + (j & 1)), (j >> 1) & 1);
         if (!ok) break;
         const int first = k_len - kbase;
         uint8_t* vt = smem + kOffKV + (j & 1) * kStage + kKTile;
