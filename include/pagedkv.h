@@ -229,6 +229,9 @@ PKV_API int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, con
                                    uint16_t* out, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Device workspace bytes pkv_paged_prefill needs (a work counter, padded). */
+#define PKV_PREFILL_WORKSPACE_BYTES 256
+
 /*
  * Varlen causal paged prefill [P1 PagedAttention; P3 prefix-cache hits share blocks].
  * Sequence b has q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens (rows cu_seqlens_q[b] ..
@@ -245,15 +248,21 @@ PKV_API int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, con
  *       NULL: there is no prefix (cu_seqlens_k must equal cu_seqlens_q) and keys are read from
  *       k and v directly; k_cache and v_cache may then be NULL.
  *   out           device, [total_q, num_q_heads, head_dim] bf16
+ *   workspace     device, >= PKV_PREFILL_WORKSPACE_BYTES, 16-byte aligned, owned by the caller;
+ *                 need not be initialised (the call zeroes its counter on `stream` before the
+ *                 kernel). Calls that may run at the same time need distinct workspaces.
+ *                 Fewer bytes return PKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  * Runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory); supports
- * head_dim 128 and group sizes 1, 2, 4, 8 (other shapes return PKV_ERR_UNSUPPORTED).
+ * head_dim 128 and group sizes 1, 2, 4, 8 (other shapes return PKV_ERR_UNSUPPORTED). A persistent
+ * grid (two CTAs per SM) claims (sequence, kv head, query tile) items from the counter.
  */
 PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
                       int32_t total_q, int32_t max_seqlen_q, const int32_t* block_tables,
                       int32_t max_blocks_per_seq, const uint16_t* k_cache,
                       const uint16_t* v_cache, pkv_cache_desc cache, int32_t num_q_heads,
-                      float scale, uint16_t* out, void* stream);
+                      float scale, uint16_t* out, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /*
  * Read and clear the device error word of the current device (PKV_DEVERR_* bits). Synchronises

@@ -75,7 +75,7 @@ def _load():
                                          i32, f32, ctypes.POINTER(DecodePlan), vp, vp, sz, vp]
     L.pkv_paged_prefill.restype = ctypes.c_int
     L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp,
-                                    CacheDesc, i32, f32, vp, vp]
+                                    CacheDesc, i32, f32, vp, vp, sz, vp]
     L.pkv_copy_blocks.restype = ctypes.c_int
     L.pkv_copy_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, vp]
     L.pkv_gather_blocks.restype = ctypes.c_int
@@ -244,9 +244,25 @@ def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_ta
     return out
 
 
+PREFILL_WORKSPACE_BYTES = 256  # PKV_PREFILL_WORKSPACE_BYTES
+_prefill_ws: dict = {}
+
+
+def prefill_workspace(device: torch.device) -> torch.Tensor:
+    """The per-device default prefill workspace (a work counter). Calls that may overlap on
+    different streams should each pass their own workspace."""
+    key = torch.device(device).index
+    with _ws_lock:
+        ws = _prefill_ws.get(key)
+        if ws is None:
+            ws = torch.empty(PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+            _prefill_ws[key] = ws
+        return ws
+
+
 def paged_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, block_tables, scale: float,
                   k_cache=None, v_cache=None, out=None, max_seqlen_q: Optional[int] = None,
-                  stream=None):
+                  workspace: Optional[torch.Tensor] = None, stream=None):
     """Varlen causal prefill. With block_tables, every key is read through the table (store the
     new tokens with kv_store first); without, keys come from k and v and there is no prefix."""
     _need(q, "q", torch.bfloat16, 3)
@@ -271,10 +287,14 @@ def paged_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, block_tables, scale: floa
     _need(out, "out", torch.bfloat16, 3)
     if max_seqlen_q is None:
         max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
+    if workspace is None:
+        workspace = prefill_workspace(q.device)
     _check(lib.pkv_paged_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                  cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Tq,
                                  int(max_seqlen_q), bt_ptr, mb, kc_ptr, vc_ptr, desc, Hq,
-                                 float(scale), out.data_ptr(), _stream_ptr(stream)))
+                                 float(scale), out.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)))
     return out
 
 

@@ -415,7 +415,8 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       int32_t total_q, int32_t max_seqlen_q, const int32_t* block_tables,
                       int32_t max_blocks_per_seq, const uint16_t* k_cache,
                       const uint16_t* v_cache, pkv_cache_desc cache, int32_t num_q_heads,
-                      float scale, uint16_t* out, void* stream) {
+                      float scale, uint16_t* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
   g_last_error[0] = 0;
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0)
     return fail(PKV_ERR_INVALID_ARG, "num_seqs, total_q and max_seqlen_q must be >= 0");
@@ -431,6 +432,11 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     return fail(PKV_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(PKV_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (!workspace || !aligned16(workspace))
+    return fail(PKV_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
+  if (workspace_bytes < PKV_PREFILL_WORKSPACE_BYTES)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace_bytes %zu < %d", workspace_bytes,
+                PKV_PREFILL_WORKSPACE_BYTES);
   const bool paged = block_tables != nullptr;
   if (paged) {
     st = check_cache(cache);
@@ -483,6 +489,7 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   a.scale = scale;
   a.out = out;
   a.flags = d.flags;
+  a.item_counter = static_cast<int32_t*>(workspace);
   cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d.num_sms,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");

@@ -87,6 +87,7 @@ struct PrefillArgs {
   float scale;
   uint16_t* out;
   int* flags;
+  int32_t* item_counter;  // device, in the caller's workspace
 };
 
 // Query positions per 128-row prefill tile, and rows per K/V TMA box.

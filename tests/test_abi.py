@@ -122,10 +122,20 @@ def test_decode_validation_without_launch(pk):
 
 def test_prefill_validation_without_launch(pk):
     d = _desc(pk)
+    ws, wsb = 4096, pk.PREFILL_WORKSPACE_BYTES
     assert pk.lib.pkv_paged_prefill(None, None, None, None, None, 0, 0, 0, None, 0, None, None,
-                                    d, 32, 0.1, None, None) in (0, -2)
+                                    d, 32, 0.1, None, None, 0, None) in (0, -2)
     assert pk.lib.pkv_paged_prefill(None, 256, 256, 256, 256, 2, 10, 5, None, 0, None, None,
-                                    d, 32, 0.1, 256, None) in (-1, -2)
+                                    d, 32, 0.1, 256, ws, wsb, None) in (-1, -2)
+    # a missing, misaligned or short workspace is refused before anything is launched
+    assert pk.lib.pkv_paged_prefill(256, 256, 256, 256, 256, 2, 10, 5, None, 0, None, None,
+                                    d, 32, 0.1, 256, None, wsb, None) == -1
+    assert b"workspace" in pk.lib.pkv_last_error()
+    assert pk.lib.pkv_paged_prefill(256, 256, 256, 256, 256, 2, 10, 5, None, 0, None, None,
+                                    d, 32, 0.1, 256, ws + 8, wsb, None) == -1
+    assert pk.lib.pkv_paged_prefill(256, 256, 256, 256, 256, 2, 10, 5, None, 0, None, None,
+                                    d, 32, 0.1, 256, ws, wsb - 1, None) == -3
+    assert b"workspace_bytes" in pk.lib.pkv_last_error()
 
 
 def test_binding_refuses_cpu_tensors(pk):
