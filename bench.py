@@ -285,7 +285,11 @@ def prefill_arm(args, torch, pk, device):
             "data": "synthetic", "config": {"workload": "prefix_prefill", "num_seqs": 64,
                                             "new_tokens": ps.tokens, "prefix": 1024},
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tf / peak, "peak_source": kind},
+                         "frac": tf / peak, "peak_source": kind,
+                         "traffic": profiled_traffic(
+                             "paged_prefill_prefix",
+                             os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc",
+                                          "paged_prefill.cu"))},
             "device_error_flags": pk.get_device_error()}
     print(json.dumps(line), flush=True)
     return 0
