@@ -93,21 +93,21 @@ struct Traits {
   static constexpr int kQBytes = GH * D * 2;
   // acc [GH][D], then m [GH], then l [GH]; padded so every warp's slot is 16-byte aligned
   static constexpr int kCbFloats = (GH * D + 2 * GH + 3) / 4 * 4;
-  // Two CTAs per SM: keep each CTA within 112 KB of shared memory.
-  static constexpr int kSmemBudget = 112 * 1024;
+  // Two CTAs per SM: keep each CTA within 113 KB of shared memory (three K+V stages at D=128).
+  static constexpr int kSmemBudget = 113 * 1024;
   static constexpr int kFixedBytes =
-      2 * kWarps * kCbFloats * 4 + kWarps * kChunks * 4 * 8 * GH * 8 + 8 * 32 + 160;
+      kWarps * kCbFloats * 4 + kWarps * kChunks * 4 * 8 * GH * 4 + 8 * 32 + 160;
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / (kStageBytes + kQBytes);
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kMaxSub = kTileT / 16;        // TMA boxes per tile at block_size 16
-  // Per-warp copy of the item's q, pre-scaled fp32 pairs: for (chunk c, word w) the 8 lanes of a
-  // group read consecutive 16-byte slots (two heads' pairs each), conflict-free.
-  static constexpr int kQfBytesPerWarp = kChunks * 4 * 8 * GH * 8;
+  // Per-warp copy of the item's q as bf16 pairs: for (chunk c, word w) lane j of a group reads
+  // the GH heads' pairs as one 4*GH-byte slot; the 8 slots are consecutive, conflict-free.
+  static constexpr int kQfBytesPerWarp = kChunks * 4 * 8 * GH * 4;
   static constexpr int kOffTiles = 0;
   static constexpr int kOffQ = kOffTiles + kStages * kStageBytes;
   static constexpr int kOffQf = kOffQ + kStages * kQBytes;
   static constexpr int kOffCb = kOffQf + kWarps * kQfBytesPerWarp;
-  static constexpr int kOffMeta = kOffCb + 2 * kWarps * kCbFloats * 4;
+  static constexpr int kOffMeta = kOffCb + kWarps * kCbFloats * 4;
   static constexpr int kOffBar = (kOffMeta + kStages * (int)sizeof(StageMeta) + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
   static_assert(kTPG * GH == kN && (kN == 8 || kN == 16), "lane-group pair layout");
@@ -115,6 +115,7 @@ struct Traits {
   static_assert(kQBytes % 16 == 0 && kOffQ % 128 == 0 && kOffCb % 16 == 0, "smem alignment");
   static_assert(kOffMeta % 16 == 0 && kOffBar % 16 == 0, "smem alignment");
   static_assert(kStageBytes % 1024 == 0 && kTileBytes % 1024 == 0, "TMA destinations");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -282,7 +283,9 @@ __global__ void __maxnreg__(168)
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + T::kOffMeta);
   const uint32_t full0 = smem_addr(smem + T::kOffBar);
   const uint32_t empty0 = full0 + T::kStages * 8;
-  const uint32_t cmb0 = empty0 + T::kStages * 8;
+  // combine: all warps wrote their partials (cmb) / all warps finished reading them (cmr)
+  const uint32_t cmb = empty0 + T::kStages * 8;
+  const uint32_t cmr = cmb + 8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -292,8 +295,8 @@ __global__ void __maxnreg__(168)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, T::kWarps);
     }
-    mbar_init(cmb0, T::kWarps);
-    mbar_init(cmb0 + 8, T::kWarps);
+    mbar_init(cmb, T::kWarps);
+    mbar_init(cmr, T::kWarps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -490,31 +493,30 @@ __global__ void __maxnreg__(168)
       for (int r = 0; r < VPL; ++r) l_lane[r] = 0.f;
     }
     if (mflags & kMetaFirst) {
-      // q of this item, scaled by scale*log2(e), into this warp's copy (lanes of group 0 write)
+      // q of this item into this warp's copy, regrouped so that a lane reads the GH heads'
+      // pairs of one (chunk, word) at once (lanes of group 0 write)
       if (lane < 8) {
         const uint8_t* qs = qbuf + st * T::kQBytes;
-        const uint64_t sc2 = pack2(p.qk_scale_log2, p.qk_scale_log2);
 #pragma unroll
         for (int c = 0; c < T::kChunks; ++c) {
-          uint64_t qv[GH][4];
+          uint32_t qv[GH][4];
 #pragma unroll
           for (int h = 0; h < GH; ++h) {
             const uint4 w = *reinterpret_cast<const uint4*>(qs + (h * D + (j + 8 * c) * 8) * 2);
-            qv[h][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
-            qv[h][1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
-            qv[h][2] = fmul2(bf16x2_to_f32x2(w.z), sc2);
-            qv[h][3] = fmul2(bf16x2_to_f32x2(w.w), sc2);
+            qv[h][0] = w.x;
+            qv[h][1] = w.y;
+            qv[h][2] = w.z;
+            qv[h][3] = w.w;
           }
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            uint8_t* base = qfw + (c * 4 + w) * (64 * GH);
+            uint8_t* base = qfw + (c * 4 + w) * (32 * GH) + j * (4 * GH);
             if constexpr (GH == 1) {
-              *reinterpret_cast<uint64_t*>(base + j * 8) = qv[0][w];
+              *reinterpret_cast<uint32_t*>(base) = qv[0][w];
+            } else if constexpr (GH == 2) {
+              *reinterpret_cast<uint2*>(base) = make_uint2(qv[0][w], qv[1][w]);
             } else {
-#pragma unroll
-              for (int hh = 0; hh < GH / 2; ++hh)
-                *reinterpret_cast<ulonglong2*>(base + hh * 128 + j * 16) =
-                    make_ulonglong2(qv[2 * hh][w], qv[2 * hh + 1][w]);
+              *reinterpret_cast<uint4*>(base) = make_uint4(qv[0][w], qv[1][w], qv[2][w], qv[3][w]);
             }
           }
         }
@@ -587,16 +589,19 @@ __global__ void __maxnreg__(168)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           uint64_t qv[GH];
-          const uint8_t* base = qfw + (c * 4 + w) * (64 * GH);
+          const uint8_t* base = qfw + (c * 4 + w) * (32 * GH) + j * (4 * GH);
           if constexpr (GH == 1) {
-            qv[0] = *reinterpret_cast<const uint64_t*>(base + j * 8);
+            qv[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(base));
+          } else if constexpr (GH == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(base);
+            qv[0] = bf16x2_to_f32x2(v.x);
+            qv[1] = bf16x2_to_f32x2(v.y);
           } else {
-#pragma unroll
-            for (int hh = 0; hh < GH / 2; ++hh) {
-              const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(base + hh * 128 + j * 16);
-              qv[2 * hh] = v.x;
-              qv[2 * hh + 1] = v.y;
-            }
+            const uint4 v = *reinterpret_cast<const uint4*>(base);
+            qv[0] = bf16x2_to_f32x2(v.x);
+            qv[1] = bf16x2_to_f32x2(v.y);
+            qv[2] = bf16x2_to_f32x2(v.z);
+            qv[3] = bf16x2_to_f32x2(v.w);
           }
 #pragma unroll
           for (int tt = 0; tt < T::kTPG; ++tt) {
@@ -622,7 +627,7 @@ __global__ void __maxnreg__(168)
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
         valid[r] = (tbase + my_t(r)) < n_valid;
-        sc[r] = valid[r] ? part[r] : -INFINITY;
+        sc[r] = valid[r] ? part[r] * p.qk_scale_log2 : -INFINITY;  // log2 units
         mx[r] = max_over_tokens<T::kN, GH>(sc[r]);
       }
 
@@ -721,8 +726,12 @@ __global__ void __maxnreg__(168)
     float l_all[GH];
 #pragma unroll
     for (int h = 0; h < GH; ++h) l_all[h] = __shfl_sync(kFullMask, l_sum[h % VPL], h / VPL);
-    const int par = item & 1;
-    float* cbw = cb + (par * T::kWarps + warp) * T::kCbFloats;
+    float* cbw = cb + warp * T::kCbFloats;
+    // every warp has finished reading the previous item's partials before this slot is reused
+    if (item > 0 && !mbar_wait(cmr, (item - 1) & 1)) {
+      if (lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+      return;
+    }
     if (g == 0) {
 #pragma unroll
       for (int h = 0; h < GH; ++h)
@@ -743,12 +752,12 @@ __global__ void __maxnreg__(168)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(cmb0 + 8 * par);
-    if (!mbar_wait(cmb0 + 8 * par, (item >> 1) & 1)) {
+    if (lane == 0) mbar_arrive(cmb);
+    if (!mbar_wait(cmb, item & 1)) {
       if (lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
       return;
     }
-    const float* cbp = cb + par * T::kWarps * T::kCbFloats;
+    const float* cbp = cb;
     const bool final_out = mt.nsplit == 1;
     // Warp w writes outputs o = 64 w + 2 lane + 256 k: one (head, 64-dim slice) per k.
     for (int o = 64 * warp + 2 * lane; o < GH * D; o += T::kWarps * 64) {
@@ -780,6 +789,8 @@ __global__ void __maxnreg__(168)
         if (lane == 0) p.part_ml[pi * (D / 64) + d / 64] = make_float2(M, den);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cmr);  // this warp no longer reads the partials
     if (!final_out) {
       // Chunk partials are out; the warp that finishes last for this (sequence, head group,
       // slice) merges all chunks: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
