@@ -110,6 +110,8 @@ SHAPES = [  # (B, Hq, Hkv, D, BS, ctx_lo, ctx_hi)
     (4, 64, 8, 128, 32, 1, 500),     # G = 8 (two CTAs of four heads per kv head)
     (5, 8, 2, 64, 64, 30, 260),      # D = 64, G = 4
     (3, 4, 4, 64, 128, 1, 140),      # D = 64, G = 1
+    (4, 8, 4, 64, 256, 1, 600),      # D = 64, G = 2
+    (5, 32, 8, 128, 128, 60, 1100),  # G = 4, BS = 128
 ]
 
 

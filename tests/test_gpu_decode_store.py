@@ -33,6 +33,8 @@ CASES = [  # (B, Hq, Hkv, D, BS, lo, hi, zero_rows, split)
     (5, 16, 8, 128, 64, 1, 400, (), -1),
     (4, 64, 8, 128, 16, 10, 3000, (1,), 256),   # G = 8, split
     (6, 8, 2, 64, 16, 1, 200, (0,), 0),        # D = 64
+    (5, 8, 8, 128, 32, 1, 500, (), 0),         # G = 1 (one CTA per SM instance)
+    (4, 8, 4, 64, 128, 5, 300, (3,), -1),      # D = 64, G = 2, auto split
 ]
 
 
