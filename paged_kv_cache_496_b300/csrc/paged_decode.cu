@@ -11,13 +11,16 @@
 //    host never synchronises; a persistent grid claims items with an atomic counter and keeps
 //    its TMA pipeline full across item boundaries.
 //  * Warp specialisation: one producer warp walks the block table (32 entries per coalesced
-//    load, kept in registers) and issues one 3-D TMA box per (block, tile) for K and for V into a
-//    multi-stage shared-memory ring guarded by mbarriers; four consumer warps compute.
-//  * Consumers: eight lanes share one token row (each lane owns D/8 of the dims), 8/GH tokens per
-//    lane group, so the q.k partial sums of 8 (token, head) pairs are reduced with a 7-shuffle
-//    reduce-scatter that leaves exactly one score per lane. Online softmax runs in log2 units in
-//    fp32 with a lazy rescale (only when a head's max grows by more than 2^8); products use the
-//    packed fp32x2 FMA. The four warps' partial (max, sum, acc) are merged through shared memory.
+//    load, kept in registers, the next 32 prefetched) and issues one 3-D TMA box per (block, tile)
+//    for K and for V into a multi-stage shared-memory ring guarded by mbarriers (three stages at
+//    D=128 with two CTAs per SM); four consumer warps compute.
+//  * Consumers: eight lanes share one token row (each lane owns D/8 of the dims). A lane group
+//    holds N (token, head) pairs (16 for groups of four heads, else 8); their q.k partial sums are
+//    reduced with a reduce-scatter that leaves N/8 full scores per lane. q comes from a per-warp
+//    bf16 copy and the scale is applied to the reduced scores. Online softmax runs in log2 units
+//    in fp32 with a lazy rescale (only when a head's max grows by more than 2^8); products use
+//    the packed fp32x2 FMA. The four warps' partial (max, sum, acc) are merged through one
+//    shared-memory buffer, guarded so that no warp overwrites it before all have read it.
 //  * Long contexts are cut into chunks (flash-decoding split). The plan kernel picks the chunk
 //    length from the actual total work (so a few long sequences are spread over all SMs while a
 //    large batch is not split at all). A chunk writes fp32 partials (un-normalised acc, running
