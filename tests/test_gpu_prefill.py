@@ -75,7 +75,7 @@ def test_prefill_no_prefix_varlen(orc, qlens):
     assert_attn_close(out, ref, what=f"no prefix {qlens}")
 
 
-@pytest.mark.parametrize("BS", [256, 64, 16])
+@pytest.mark.parametrize("BS", [256, 128, 64, 32, 16])
 @pytest.mark.parametrize("q_scale", [1.0, 8.0], ids=["normal", "sharp"])
 def test_prefill_shared_prefix(orc, BS, q_scale):
     case = W.prefix_prefill_case(63, 4, 256, 1, 300, 32, 8, 128, BS, q_scale=q_scale,
