@@ -273,6 +273,53 @@ __device__ __forceinline__ float sum_over_tokens(float x) {
   return x;
 }
 
+// The last warp to finish a (sequence, head group, output slice) of a split sequence merges all
+// chunk partials: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s, in one pass with a running
+// max and eight chunks' loads in flight. Out of line: it runs once per split sequence, and the
+// decode loop runs faster with less code in it.
+template <int D, int GH, int kWarps>
+__device__ __noinline__ void merge_chunks(const DecodeParams& p, int b, int x, int nsplit, int warp,
+                                          int lane) {
+  for (int o = 64 * warp + 2 * lane; o < GH * D; o += kWarps * 64) {
+    const int h = o / D, d = o % D;
+    const int head = x * GH + h;
+    const int64_t base = (int64_t)b * p.max_splits * p.num_q_heads + head;
+    float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
+    for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
+      float2 ml[8], a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ml[u] = make_float2(-INFINITY, 0.f);
+        a[u] = make_float2(0.f, 0.f);
+        if (sp0 + u < nsplit) {
+          const int64_t pi = base + (int64_t)(sp0 + u) * p.num_q_heads;
+          ml[u] = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
+          a[u] = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
+        }
+      }
+      float mnew = M;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mnew = fmaxf(mnew, ml[u].x);
+      if (mnew == -INFINITY) continue;
+      const float keep = M == -INFINITY ? 0.f : fast_exp2(M - mnew);
+      den *= keep;
+      n0 *= keep;
+      n1 *= keep;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wt = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mnew);
+        den += wt * ml[u].y;
+        n0 += wt * a[u].x;
+        n1 += wt * a[u].y;
+      }
+      M = mnew;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)b * p.num_q_heads + head) * D + d) =
+        __floats2bfloat162_rn(n0 * inv, n1 * inv);
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // The decode kernel
 // ---------------------------------------------------------------------------------------------
@@ -812,46 +859,7 @@ __global__ void __maxnreg__(168)
       done = __shfl_sync(kFullMask, done, 0);
       if (done == (uint32_t)mt.nsplit - 1) {
         __threadfence();
-        for (int o = 64 * warp + 2 * lane; o < GH * D; o += T::kWarps * 64) {
-          const int h = o / D, d = o % D;
-          const int head = mt.x * GH + h;
-          const int64_t base = (int64_t)mt.b * p.max_splits * p.num_q_heads + head;
-          // one pass with a running max, eight chunks' loads in flight at a time
-          float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
-          for (int sp0 = 0; sp0 < mt.nsplit; sp0 += 8) {
-            float2 ml[8], a[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              ml[u] = make_float2(-INFINITY, 0.f);
-              a[u] = make_float2(0.f, 0.f);
-              if (sp0 + u < mt.nsplit) {
-                const int64_t pi = base + (int64_t)(sp0 + u) * p.num_q_heads;
-                ml[u] = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
-                a[u] = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
-              }
-            }
-            float mnew = M;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mnew = fmaxf(mnew, ml[u].x);
-            if (mnew == -INFINITY) continue;
-            const float keep = M == -INFINITY ? 0.f : fast_exp2(M - mnew);
-            den *= keep;
-            n0 *= keep;
-            n1 *= keep;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float wt = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mnew);
-              den += wt * ml[u].y;
-              n0 += wt * a[u].x;
-              n1 += wt * a[u].y;
-            }
-            M = mnew;
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)mt.b * p.num_q_heads + head) *
-                                                         D + d) =
-              __floats2bfloat162_rn(n0 * inv, n1 * inv);
-        }
+        merge_chunks<D, GH, T::kWarps>(p, mt.b, mt.x, mt.nsplit, warp, lane);
       }
     }
     ++item;
