@@ -324,9 +324,8 @@ __device__ __noinline__ void merge_chunks(const DecodeParams& p, int b, int x, i
 // The decode kernel
 // ---------------------------------------------------------------------------------------------
 
-// kFuse: the decode of pkv_paged_decode_store (the newest token is written to the cache by the
-// kernel). A separate instantiation keeps that code out of the plain decode's hot loop, which
-// measured 3-4% faster without it.
+// kFuse: the decode of pkv_paged_decode_store. The producer warp writes the step's new token to
+// the cache before the copies that read it, so the consumers are the same as the plain decode's.
 template <int D, int GH, bool kFuse>
 __global__ void __maxnreg__(168)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -427,6 +426,35 @@ __global__ void __maxnreg__(168)
       const uint16_t* qsrc = p.q + ((int64_t)b * p.num_q_heads + x * GH) * D;
       const int kv_head = x / p.groups_per_kv;
 
+      if constexpr (kFuse) {
+        // The fused store: this item holds position ctx - 1, so write the step's new token (this
+        // kv head's K and V rows) to its slot before issuing the copies that read it. Every head
+        // group of the kv head writes the same bytes.
+        if (s == nsplit - 1) {
+          constexpr int kRowChunks = D / 8;  // 16-byte chunks of one row
+          const int slot = __ldg(p.slot_mapping + b);
+          const bool writes = slot >= 0 && slot < p.num_blocks * bs;
+          if (writes && lane < 2 * kRowChunks) {
+            const bool is_k = lane < kRowChunks;
+            const int c16 = lane % kRowChunks;
+            const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                (is_k ? p.k_new : p.v_new) + ((int64_t)b * p.num_kv_heads + kv_head) * D + c16 * 8));
+            *reinterpret_cast<uint4*>((is_k ? p.k_cache : p.v_cache) +
+                                      ((int64_t)slot * p.num_kv_heads + kv_head) * D + c16 * 8) =
+                val;
+            fence_proxy_async_global();
+          }
+          if (lane == 0 && slot != -1) {
+            const int pos = ctx - 1;
+            const int e = pos / bs;
+            const int blk = e < p.max_blocks ? __ldg(bt_row + e) : -1;
+            if (!writes || slot != blk * bs + pos % bs) raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
+          }
+          __syncwarp();
+          fence_proxy_async_global();  // lane 0 issues the copies that read the row
+        }
+      }
+
       for (int tok0 = tok_begin; tok0 < tok_end && ok; tok0 += T::kTileT) {
         const int st = issue % T::kStages;
         const int e0 = tok0 / bs;
@@ -520,14 +548,6 @@ __global__ void __maxnreg__(168)
   for (int r = 0; r < VPL; ++r) l_lane[r] = 0.f;
   uint32_t use = 0;
   uint32_t item = 0;
-  // fused store: this warp owns the newest token's row in the item's last tile
-  int fuse_row = -1;   // row of the newest token in the last tile (this warp's), or -1
-  int fuse_g = 0;      // its kv head
-  int fuse_pos = 0;    // its position in the sequence
-  int fuse_slot = -1;  // where it goes in the cache (-1: this CTA does not write it)
-  int fuse_blk = 0;    // block table entry of fuse_pos, to check the slot against
-  uint4 fuse_val = make_uint4(0u, 0u, 0u, 0u);
-  constexpr int kRowChunks = D / 8;  // 16-byte chunks of one (token, kv head) row
 
   while (true) {
     const int st = use % T::kStages;
@@ -578,50 +598,6 @@ __global__ void __maxnreg__(168)
         }
       }
       __syncwarp();
-      // Fused store: the loads are issued now and used only at the item's last tile.
-      fuse_row = -1;
-      if (kFuse && meta[st].split == meta[st].nsplit - 1) {
-        const int b = meta[st].b, x = meta[st].x;
-        const int pos = meta[st].tok_end - 1;  // the last chunk ends at the context length
-        const int r = pos % T::kTileT;
-        if (r / T::kTokPerWarp == warp) {
-          fuse_row = r;
-          fuse_pos = pos;
-          fuse_g = x / p.groups_per_kv;
-          if (lane < 2 * kRowChunks) {
-            const uint16_t* src = (lane < kRowChunks ? p.k_new : p.v_new) +
-                                  ((int64_t)b * p.num_kv_heads + fuse_g) * D +
-                                  (lane % kRowChunks) * 8;
-            fuse_val = __ldg(reinterpret_cast<const uint4*>(src));
-          }
-          fuse_slot = -1;
-          if (x % p.groups_per_kv == 0) {  // one head group per kv head writes the cache
-            fuse_slot = __ldg(p.slot_mapping + b);
-            fuse_blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks + pos / p.block_size);
-          }
-        }
-      }
-    }
-
-    if (kFuse && fuse_row >= 0 && (mflags & kMetaLast)) {
-      // put the newest token into the landed tile (the cache copy may not be written yet)
-      const bool writes = fuse_slot >= 0 && fuse_slot < p.num_blocks * p.block_size;
-      if (lane < 2 * kRowChunks) {
-        uint8_t* dst = tiles + st * T::kStageBytes + (lane < kRowChunks ? 0 : T::kTileBytes) +
-                       fuse_row * T::kRowBytes + (lane % kRowChunks) * 16;
-        *reinterpret_cast<uint4*>(dst) = fuse_val;
-        if (writes)
-          *reinterpret_cast<uint4*>((lane < kRowChunks ? p.k_cache : p.v_cache) +
-                                    ((int64_t)fuse_slot * p.num_kv_heads + fuse_g) * D +
-                                    (lane % kRowChunks) * 8) = fuse_val;
-      }
-      if (lane == 0 && fuse_slot != -1) {
-        const int expect = fuse_blk * p.block_size + fuse_pos % p.block_size;
-        if (!writes || fuse_slot != expect) raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
-      }
-      fence_async_shared_cta();  // the stage will be refilled by TMA later
-      __syncwarp();
-      fuse_row = -1;
     }
 
     if (!(mflags & kMetaZero)) {
