@@ -49,12 +49,6 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA, tensor
-// core) accesses of the same bytes.
-__device__ __forceinline__ void fence_async_shared_cta() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Order this thread's generic-proxy global writes before its later async-proxy (TMA) reads of
 // the same bytes.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -124,14 +118,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Named barrier over a subset of warps
-// ---------------------------------------------------------------------------------------------
-
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// ---------------------------------------------------------------------------------------------
 // Packed fp32x2 arithmetic (one instruction for two lanes of data) and bf16 unpacking
 // ---------------------------------------------------------------------------------------------
 
@@ -159,12 +145,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 // A 32-bit word holding two bf16 values (element 2i in the low half) -> the same two values as
 // an fp32 pair. Exact: a bf16 is the upper half of the fp32 with the same value.
 __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
@@ -176,14 +156,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
 }
 
 }  // namespace pkv
