@@ -130,6 +130,7 @@ constexpr int kPlanThreads = 1024;
 // write, final merge) more often than they gain in balance: on a B300, 4 x 32768 + 60 short
 // sequences run 16% faster at 2048-token chunks than at 512.
 constexpr double kChunkShare = 0.4;
+constexpr int kSizeBuckets = 32;  // length classes of the remainder items (longest-first order)
 
 struct PlanParams {
   const int32_t* context_lens;
@@ -208,22 +209,57 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
   }
   __syncthreads();
   const int32_t S = split_sh;
-  uint32_t local = 0;
+  // Items in roughly longest-first order, so the last claims are the smallest: first every
+  // full-length chunk, then the remainders (a split sequence's last, partial chunk and every
+  // unsplit sequence) by decreasing length, in kSizeBuckets buckets; items of context 0 last.
+  __shared__ uint32_t bucket_count[kSizeBuckets + 1], bucket_next[kSizeBuckets + 1];
+  if (tid <= kSizeBuckets) bucket_count[tid] = 0u;
+  uint32_t local_full = 0;
   for (int b = b0; b < b1; ++b) {
     const int ctx = min(pp.context_lens[b], pp.cap_tokens);
-    local += ctx > 0 ? (uint32_t)((ctx + S - 1) / S) : 1u;
-  }
-  uint32_t total = 0;
-  uint32_t pos = block_exclusive_scan(local, warp_sums, &total);
-  for (int b = b0; b < b1; ++b) {
-    const int ctx = min(pp.context_lens[b], pp.cap_tokens);
-    const int n = ctx > 0 ? (ctx + S - 1) / S : 1;
-    for (int s = 0; s < n; ++s) pp.items[pos++] = make_int2(b, s);
+    if (ctx <= 0) continue;
+    const int full = ctx / S;
+    local_full += (uint32_t)full;
     // only split sequences use merge counters
-    if (n > 1)
+    if ((ctx + S - 1) / S > 1)
       for (int i = 0; i < pp.counters_per_seq; ++i)
         pp.counters[(int64_t)b * pp.counters_per_seq + i] = 0u;
   }
+  uint32_t total_full = 0;
+  uint32_t pos = block_exclusive_scan(local_full, warp_sums, &total_full);
+  // bucket of a sequence's remainder: kSizeBuckets - 1 (longest) .. 0; context 0 -> kSizeBuckets
+  auto bucket_of = [&](int ctx) -> int {
+    if (ctx <= 0) return kSizeBuckets;
+    const int rem = ctx - (ctx / S) * S;
+    if (rem == 0) return -1;  // no remainder: all chunks are full
+    return (int)(((int64_t)rem * kSizeBuckets - 1) / S);
+  };
+  for (int b = b0; b < b1; ++b) {
+    const int ctx = min(pp.context_lens[b], pp.cap_tokens);
+    const int full = ctx > 0 ? ctx / S : 0;
+    for (int s = 0; s < full; ++s) pp.items[pos++] = make_int2(b, s);
+    const int k = bucket_of(ctx);
+    if (k >= 0) atomicAdd(&bucket_count[k], 1u);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t at = total_full;
+    for (int k = kSizeBuckets - 1; k >= 0; --k) {
+      bucket_next[k] = at;
+      at += bucket_count[k];
+    }
+    bucket_next[kSizeBuckets] = at;
+  }
+  __syncthreads();
+  for (int b = b0; b < b1; ++b) {
+    const int ctx = min(pp.context_lens[b], pp.cap_tokens);
+    const int k = bucket_of(ctx);
+    if (k < 0) continue;
+    const uint32_t at = atomicAdd(&bucket_next[k], 1u);
+    pp.items[at] = make_int2(b, ctx > 0 ? ctx / S : 0);
+  }
+  uint32_t total = total_full;
+  for (int k = 0; k <= kSizeBuckets; ++k) total += bucket_count[k];
   if (tid == 0) {
     pp.header[1] = total;  // number of (sequence, chunk) items
     pp.header[0] = 0u;     // claim counter
