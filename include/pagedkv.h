@@ -285,7 +285,8 @@ PKV_API const char* pkv_status_string(int status);
 /* Message for the last failing call on this thread ("" if none). */
 PKV_API const char* pkv_last_error(void);
 
-/* ABI version: major * 10000 + minor * 100 + patch. */
+/* ABI version: major * 10000 + minor * 100 + patch. 0.2.0 added the prefill workspace. */
+#define PKV_VERSION 200
 PKV_API int pkv_version(void);
 
 #ifdef __cplusplus

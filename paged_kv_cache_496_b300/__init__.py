@@ -57,6 +57,9 @@ class PagedKVError(RuntimeError):
         self.status = status
 
 
+ABI_VERSION = 200  # PKV_VERSION of include/pagedkv.h that the argtypes below describe
+
+
 def _load():
     if not os.path.exists(LIBRARY):
         raise ImportError(f"{LIBRARY} is missing: build it with `python "
@@ -94,6 +97,9 @@ def _load():
     L.pkv_last_error.argtypes = []
     L.pkv_version.restype = ctypes.c_int
     L.pkv_version.argtypes = []
+    if L.pkv_version() != ABI_VERSION:
+        raise ImportError(f"{LIBRARY} has ABI version {L.pkv_version()}, this binding declares "
+                          f"{ABI_VERSION}: rebuild it with `python paged_kv_cache_496_b300/build.py`")
     return L
 
 

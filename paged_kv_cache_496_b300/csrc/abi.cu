@@ -155,7 +155,7 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return PKV_VERSION; }
 
 const char* pkv_last_error(void) { return g_last_error; }
 
