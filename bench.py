@@ -543,7 +543,7 @@ def main():
             "config": {"workload": args.workload, "num_seqs": step.B, "num_layers": step.L,
                        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                        "head_dim": w.head_dim, "block_size": w.block_size,
-                       "context": "input U{100..1024} + generated U{100..1024}",
+                       "context": w.description,
                        "mean_context": float(step.ctx.mean()),
                        "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
                        "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
