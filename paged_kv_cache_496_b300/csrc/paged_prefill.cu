@@ -9,13 +9,18 @@
 // Design (per CTA: one sequence, one kv head, one tile of 128 query rows):
 //  * The 128 rows are 128/G positions x the G query heads that share the kv head, so each K/V
 //    tile feeds all of them (rows ordered position-major, as the Q TMA box delivers them).
-//  * Warp 0 claims items, loads Q and streams 64-key K and V tiles through the block table with
-//    3-D TMA boxes in 128-byte swizzle (the layout the tensor core reads). K and V have their own
-//    two-deep rings and barriers, and K runs one tile ahead of V: a K buffer is free as soon as
-//    its S = Q K^T is done, so the next K is in flight while the softmax of the current tile runs.
-//  * Warp 1 allocates 256 TMEM columns and, from one thread, issues S = Q K^T (M=128, N=64,
-//    K=128: eight kind::f16 MMAs, K-major operands) into TMEM columns [0, 64) and O += P V
-//    (M=128, N=128, K=64: four MMAs, V read MN-major) into columns [64, 192).
+//  * Warp 0 claims items and streams 64-key K and V tiles through the block table with 3-D TMA
+//    boxes in 128-byte swizzle (the layout the tensor core reads). K and V have their own
+//    three-deep rings and barriers, and K runs one tile ahead of V: a K buffer is free as soon as
+//    its S = Q K^T is done. An item's Q travels through the K ring too, as two 16 KB slots of 64
+//    dims each, ahead of its first key tile. Each ring slot has its own issuing lane: one
+//    thread's bulk copies complete one barrier phase at a time (a few hundred nanoseconds each,
+//    whatever their size), so a thread with several phases in flight would queue them.
+//  * Warp 1 allocates 256 TMEM columns and, from one thread, copies Q from the ring into TMEM
+//    columns [192, 256) (tcgen05.cp), issues S = Q K^T (M=128, N=64, K=128: eight kind::f16
+//    MMAs, A from TMEM, K K-major in shared memory) into columns [0, 64) and O += P V (M=128,
+//    N=128, K=64: four MMAs, V read MN-major) into columns [64, 192). With A in TMEM an N=64 MMA
+//    reads 2 KB of shared memory instead of 6 KB and is no longer limited by that read.
 //  * Warps 2-5 (one TMEM lane quarter each, thread = query row) load S rows, apply the causal
 //    mask and an online softmax in log2 units with a lazy rescale (O in TMEM is rescaled only when
 //    a row's max grows by more than 2^8), write P as bf16 into shared memory in the swizzled
@@ -37,23 +42,23 @@ constexpr int kThreadsP = 192;
 constexpr int kTmemCols = 256;
 constexpr int kColS = 0;
 constexpr int kColO = 64;
+constexpr int kColQ = 192;  // Q as the MMA A operand: 128 lanes x 64 columns of bf16 pairs
 constexpr float kTauP = 8.0f;
 
-constexpr int kQBytes = kRows * kHD * 2;     // two 16 KB halves of 64 dims
-constexpr int kQHalf = kRows * 128;          // 16 KB
+constexpr int kQHalf = kRows * 128;          // 16 KB: 64 dims of Q, one K-ring slot
 constexpr int kKTile = kKeys * kHD * 2;      // 16 KB: two 8 KB halves
 constexpr int kKHalf = kKeys * 128;          // 8 KB
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kKStages * kKTile;
-constexpr int kOffP = kOffV + kVStages * kKTile;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
 constexpr int kPBytes = kRows * kKeys * 2;
-constexpr int kOffBar = kOffP + kPBytes;
-// barriers: q_full, q_empty, k_full[], k_empty[], v_full[], v_empty[], s_full, s_free, p_full,
-// o_done, o_free, mma_done, item_full[2], item_empty[2]
-constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarFullK = 2, kBarEmptyK = kBarFullK + kKStages,
+constexpr int kOffP = 0;
+constexpr int kOffK = kOffP + kPBytes;
+constexpr int kOffV = kOffK + kKStages * kKTile;
+constexpr int kOffBar = kOffV + kVStages * kKTile;
+static_assert(kQHalf == kKTile, "a Q half fills one K-ring slot");
+// barriers: k_full[], k_empty[], v_full[], v_empty[], s_full, s_free, p_full, o_done, o_free,
+// mma_done, item_full[2], item_empty[2]
+constexpr int kBarFullK = 0, kBarEmptyK = kBarFullK + kKStages,
               kBarFullV = kBarEmptyK + kKStages, kBarEmptyV = kBarFullV + kVStages,
               kBarSFull = kBarEmptyV + kVStages, kBarSFree = kBarSFull + 1,
               kBarPFull = kBarSFree + 1, kBarODone = kBarPFull + 1, kBarOFree = kBarODone + 1,
@@ -146,8 +151,6 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarFullK + s), 1);
       mbar_init(bar(kBarEmptyK + s), 1);
@@ -193,8 +196,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 
   if (warp == 0) {
     // =============================== producer ===============================
-    // For global tile t: (the item's Q when t is its first tile), K(t), then V(t-1); K runs one
-    // tile ahead of V.
+    // Per item: its two Q halves into the K ring, then for global tile t: K(t) and V(t-1); K runs
+    // one tile ahead of V. kr counts K-ring slots used (Q halves and key tiles). All lanes run
+    // the loop (the block-table window is spread over them); each ring slot has its own issuing
+    // lane, so that a thread never has more than one barrier phase of copies in flight.
     bool ok = true;
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
@@ -205,22 +210,38 @@ __global__ void __launch_bounds__(kThreadsP, 2)
     const int bs = p.block_size;
     const int box = p.box_rows;
     const int nsub = kKeys / box;
-    int t = 0, n = 0;
+    int t = 0, n = 0, kr = 0;
+    // cache rows and kv head of key tile t - 1
     int prev_rows[kKeys / 16];
+#pragma unroll
+    for (int sb = 0; sb < kKeys / 16; ++sb) prev_rows[sb] = 0;
     int prev_g = 0;
-    // lane 0 only: V of global tile tv from prev_rows / prev_g
-    auto issue_v = [&](int tv) -> bool {
-      const int st = tv & 1;
-      if (!mbar_wait(bar(kBarEmptyV + st), ((tv >> 1) & 1) ^ 1)) return false;
-      const uint32_t full = bar(kBarFullV + st);
+    // Lane s (s < kKStages) owns K-ring slot s and lane kKStages + s owns V-ring slot s: it waits
+    // for the slot and issues the copies into it. Unless k_on is false, the owner of K-ring slot
+    // use kr puts K of the current key tile (cache rows k_rows, kv head gk) there; unless v_on is
+    // false, the owner of the slot of V tile tv puts V (rows prev_rows, head prev_g) there.
+    // Returns the lane's success.
+    auto issue_kv = [&](const int (&k_rows)[kKeys / 16], int gk, bool k_on, int tv,
+                        bool v_on) -> bool {
+      const bool isk = k_on && lane == kr % kKStages;
+      const bool isv = v_on && lane == kKStages + tv % kVStages;
+      if (!isk && !isv) return true;
+      const int u = isk ? kr : tv;
+      const int st = isk ? u % kKStages : u % kVStages;
+      const int use = isk ? u / kKStages : u / kVStages;
+      if (!mbar_wait(bar((isk ? kBarEmptyK : kBarEmptyV) + st), (use & 1) ^ 1)) return false;
+      const uint32_t full = bar((isk ? kBarFullK : kBarFullV) + st);
       mbar_arrive_expect_tx(full, kKTile);
-      const uint32_t vd = sbase + kOffV + st * kKTile;
+      const uint32_t d = sbase + (isk ? kOffK : kOffV) + st * kKTile;
+      const CUtensorMap* map = isk ? &tmap_k : &tmap_v;
+      const int g = isk ? gk : prev_g;
 #pragma unroll
       for (int sb = 0; sb < kKeys / 16; ++sb) {
         if (sb < nsub) {
           const uint32_t off = (uint32_t)(sb * box * 128);
-          tma_load_3d(vd + off, &tmap_v, 0, prev_g, prev_rows[sb], full);
-          tma_load_3d(vd + kKHalf + off, &tmap_v, 64, prev_g, prev_rows[sb], full);
+          const int r = isk ? k_rows[sb] : prev_rows[sb];
+          tma_load_3d(d + off, map, 0, g, r, full);
+          tma_load_3d(d + kKHalf + off, map, 64, g, r, full);
         }
       }
       return true;
@@ -259,16 +280,20 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         }
         bt_row = p.block_tables + (int64_t)it.b * p.max_blocks;
       }
-      if (lane == 0) {
-        ok = mbar_wait(bar(kBarQEmpty), (n & 1) ^ 1);
+      // Q half h into K-ring slot use kr + h, from that slot's lane
+      const int hq = (lane + kKStages - kr % kKStages) % kKStages;
+      if (lane < kKStages && hq < 2) {
+        const int u = kr + hq, st = u % kKStages;
+        ok = mbar_wait(bar(kBarEmptyK + st), ((u / kKStages) & 1) ^ 1);
         if (ok) {
-          mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
-          tma_load_3d(sbase + kOffQ, &tmap_q, 0, it.g * G, it.q_start + it.q0, bar(kBarQFull));
-          tma_load_3d(sbase + kOffQ + kQHalf, &tmap_q, 64, it.g * G, it.q_start + it.q0,
-                      bar(kBarQFull));
+          const uint32_t full = bar(kBarFullK + st);
+          mbar_arrive_expect_tx(full, kKTile);
+          tma_load_3d(sbase + kOffK + st * kKTile, &tmap_q, 64 * hq, it.g * G,
+                      it.q_start + it.q0, full);
         }
       }
-      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      kr += 2;
+      ok = __all_sync(kFullMask, ok);
       int win_base = -1000000, win_val = -1;
       for (int j = 0; j < it.n_kt && ok; ++j, ++t) {
         int rows[kKeys / 16];
@@ -302,49 +327,36 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           for (int sb = 0; sb < kKeys / 16; ++sb)
             if (sb < nsub) rows[sb] = it.q_start + key0 + sb * box;
         }
-        if (lane == 0) {
-          const int st = t % kKStages;
-          ok = mbar_wait(bar(kBarEmptyK + st), ((t / kKStages) & 1) ^ 1);
-          if (ok) {
-            const uint32_t full = bar(kBarFullK + st);
-            mbar_arrive_expect_tx(full, kKTile);
-            const uint32_t kd = sbase + kOffK + st * kKTile;
-#pragma unroll
-            for (int sb = 0; sb < kKeys / 16; ++sb) {
-              if (sb < nsub) {
-                const uint32_t off = (uint32_t)(sb * box * 128);
-                tma_load_3d(kd + off, &tmap_k, 0, it.g, rows[sb], full);
-                tma_load_3d(kd + kKHalf + off, &tmap_k, 64, it.g, rows[sb], full);
-              }
-            }
-          }
-          if (ok && t > 0) ok = issue_v(t - 1);
-        }
-        ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+        if (lane < kKStages + kVStages) ok = issue_kv(rows, it.g, true, t - 1, t > 0);
+        ++kr;
+        ok = __all_sync(kFullMask, ok);
 #pragma unroll
         for (int sb = 0; sb < kKeys / 16; ++sb) prev_rows[sb] = rows[sb];
         prev_g = it.g;
       }
       ++n;
     }
+    bool v_ok = true;  // V of the last key tile
+    if (ok && t > 0) v_ok = issue_kv(prev_rows, prev_g, false, t - 1, true);
+    ok = __all_sync(kFullMask, ok && v_ok);
     if (lane == 0) {
-      if (ok && t > 0) ok = issue_v(t - 1);
       if (!ok) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
       // never leave while a copy into this CTA's shared memory may be in flight: wait for the
-      // last Q and the last K and V tiles of each ring (earlier ones completed before their slot
-      // was reused). After a timeout some of these were never issued; their waits then also time
-      // out, which is harmless.
-      bool drained = n == 0 || mbar_wait(bar(kBarQFull), (n - 1) & 1);
-      for (int i = (t > kKStages ? t - kKStages : 0); i < t && drained; ++i)
+      // last uses of each ring's slots (earlier ones completed before their slot was reused).
+      // After a timeout some of these were never issued; their waits then also time out, which
+      // is harmless.
+      bool drained = true;
+      for (int i = (kr > kKStages ? kr - kKStages : 0); i < kr && drained; ++i)
         drained = mbar_wait(bar(kBarFullK + i % kKStages), (i / kKStages) & 1);
       for (int i = (t > kVStages ? t - kVStages : 0); i < t && drained; ++i)
-        drained = mbar_wait(bar(kBarFullV + (i & 1)), (i >> 1) & 1);
+        drained = mbar_wait(bar(kBarFullV + i % kVStages), (i / kVStages) & 1);
       if (!drained) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ============================ MMA issuer (one thread) ============================
-    // For global tile t: S(t) = Q K(t)^T, then O += P(t-1) V(t-1), so the tensor core computes
-    // the next S while the softmax warps work on the current one, across item boundaries too.
+    // Per item: Q from its two K-ring slots into TMEM; then for global tile t: S(t) = Q K(t)^T,
+    // then O += P(t-1) V(t-1), so the tensor core computes the next S while the softmax warps work
+    // on the current one, across item boundaries too.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, false);
       const uint32_t idesc_o = idesc_bf16_f32(kRows, kHD, true);
@@ -353,12 +365,12 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       // after the previous item's O has been read out)
       auto issue_pv = [&](int tv, bool first, int nv) {
         if (!ok) return;
-        ok = mbar_wait(bar(kBarFullV + (tv & 1)), (tv >> 1) & 1);
+        ok = mbar_wait(bar(kBarFullV + tv % kVStages), (tv / kVStages) & 1);
         if (ok) ok = mbar_wait(bar(kBarPFull), tv & 1);
         if (ok && first && nv > 0) ok = mbar_wait(bar(kBarOFree), (nv - 1) & 1);
         if (!ok) return;
         tc_fence_after_sync();
-        const uint32_t vbase = sbase + kOffV + (tv & 1) * kKTile;
+        const uint32_t vbase = sbase + kOffV + (tv % kVStages) * kKTile;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint64_t bdesc = sdesc_mnmajor_sw128(vbase + kk * 16 * 128, kKHalf);
@@ -366,9 +378,9 @@ __global__ void __launch_bounds__(kThreadsP, 2)
                      (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kBarODone));
-        tc_commit(bar(kBarEmptyV + (tv & 1)));
+        tc_commit(bar(kBarEmptyV + tv % kVStages));
       };
-      int t = 0, n = 0;
+      int t = 0, n = 0, kr = 0;
       bool pending = false, pend_first = false;
       int pend_n = 0;
       while (ok) {
@@ -376,10 +388,23 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         if (id < 0) break;
         Item it;
         load_item(p, id, it);
-        ok = ok && mbar_wait(bar(kBarQFull), n & 1);
-        for (int j = 0; j < it.n_kt && ok; ++j, ++t) {
-          const int st = t % kKStages;
-          ok = mbar_wait(bar(kBarFullK + st), (t / kKStages) & 1);
+        // the previous item's S MMAs read Q's TMEM columns: they are complete before the copy
+        // below overwrites them (an MMA followed by a copy is not ordered by the tensor core)
+        if (ok && t > 0) ok = mbar_wait(bar(kBarSFull), (t - 1) & 1);
+        for (int h = 0; h < 2 && ok; ++h, ++kr) {
+          const int st = kr % kKStages;
+          ok = mbar_wait(bar(kBarFullK + st), (kr / kKStages) & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t qs = sbase + kOffK + st * kKTile;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_cp_128x256b(tmem + kColQ + (h * 4 + kk) * 8, sdesc_kmajor_sw128(qs + kk * 32));
+          tc_commit(bar(kBarEmptyK + st));
+        }
+        for (int j = 0; j < it.n_kt && ok; ++j, ++t, ++kr) {
+          const int st = kr % kKStages;
+          ok = mbar_wait(bar(kBarFullK + st), (kr / kKStages) & 1);
           if (ok && t > 0) ok = mbar_wait(bar(kBarSFree), (t - 1) & 1);
           if (!ok) break;
           tc_fence_after_sync();
@@ -387,13 +412,11 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk & 3) * 32);
-            const uint64_t a = sdesc_kmajor_sw128(sbase + kOffQ + (kk >> 2) * kQHalf + off);
             const uint64_t bdesc = sdesc_kmajor_sw128(kbase + (kk >> 2) * kKHalf + off);
-            tc_mma_f16(tmem + kColS, a, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+            tc_mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, bdesc, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(kBarSFull));
           tc_commit(bar(kBarEmptyK + st));
-          if (j == it.n_kt - 1) tc_commit(bar(kBarQEmpty));
           if (pending) issue_pv(t - 1, pend_first, pend_n);
           pending = true;
           pend_first = j == 0;
@@ -522,10 +545,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         if (j == it.n_kt - 1 && kbase + kKeys > it.k_len) {
           // V rows past the last key hold whatever the cache holds there: zero them (after the
           // stage's copy has landed)
-          ok = mbar_wait(bar(kBarFullV + (t & 1)), (t >> 1) & 1);
+          ok = mbar_wait(bar(kBarFullV + t % kVStages), (t / kVStages) & 1);
           if (!ok) break;
           const int first = it.k_len - kbase;
-          uint8_t* vt = smem + kOffV + (t & 1) * kKTile;
+          uint8_t* vt = smem + kOffV + (t % kVStages) * kKTile;
           const int nrow = kKeys - first;
           for (int i = threadIdx.x - 64; i < nrow * 16; i += 128) {
             const int row = first + i / 16, part16 = i % 16;  // 16 x 16 bytes = both halves

@@ -51,6 +51,25 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// ---- MMA: D[tmem] (+)= A[tmem] * B[smem]^T (A as M lanes x K/2 packed bf16 pairs per lane) ----
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 128-row x 32-byte matrix from shared memory (described like an MMA operand) into 128
+// TMEM lanes x 8 columns. A later MMA from the same thread sees the copied data; an MMA issued
+// earlier that still reads those columns is not ordered against the copy.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc)
+               : "memory");
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void tc_commit(uint32_t mbar_addr) {
   asm volatile(
