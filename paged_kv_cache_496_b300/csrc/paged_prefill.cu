@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kThreadsP, 2)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, false);
       const uint32_t idesc_o = idesc_bf16_f32(kRows, kHD, true);
+      const uint64_t adesc_p = sdesc_kmajor_sw128(sbase + kOffP);
       bool ok = true;
       // O += P V for global tile tv; `first`: the first tile of item number nv (O starts at 0,
       // after the previous item's O has been read out)
@@ -370,11 +371,13 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         if (ok && first && nv > 0) ok = mbar_wait(bar(kBarOFree), (nv - 1) & 1);
         if (!ok) return;
         tc_fence_after_sync();
-        const uint32_t vbase = sbase + kOffV + (tv % kVStages) * kKTile;
+        // descriptors advance by address / 16 in their low 14 bits (shared addresses < 256 KB)
+        const uint64_t bdesc0 =
+            sdesc_mnmajor_sw128(sbase + kOffV + (tv % kVStages) * kKTile, kKHalf);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t bdesc = sdesc_mnmajor_sw128(vbase + kk * 16 * 128, kKHalf);
-          tc_mma_f16(tmem + kColO, sdesc_kmajor_sw128(sbase + kOffP + kk * 32), bdesc, idesc_o,
+          tc_mma_f16(tmem + kColO, adesc_p + (uint64_t)(kk * 32 / 16),
+                     bdesc0 + (uint64_t)(kk * 16 * 128 / 16), idesc_o,
                      (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kBarODone));
@@ -408,11 +411,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           if (ok && t > 0) ok = mbar_wait(bar(kBarSFree), (t - 1) & 1);
           if (!ok) break;
           tc_fence_after_sync();
-          const uint32_t kbase = sbase + kOffK + st * kKTile;
+          const uint64_t kdesc0 = sdesc_kmajor_sw128(sbase + kOffK + st * kKTile);
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk & 3) * 32);
-            const uint64_t bdesc = sdesc_kmajor_sw128(kbase + (kk >> 2) * kKHalf + off);
+            const uint64_t bdesc = kdesc0 + (uint64_t)(((kk >> 2) * kKHalf + (kk & 3) * 32) / 16);
             tc_mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, bdesc, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(kBarSFull));
