@@ -473,14 +473,13 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 #pragma unroll
           for (int c = 8; c < 64; ++c) part[c & 7] = fmaxf(part[c & 7], __uint_as_float(sr[c]));
         } else {
+          // keys kbase + c with c < nv are unmasked for this row (c <= limit - kbase, inside k_len)
+          const int nv = max(0, min(kKeys, min(limit + 1, it.k_len) - kbase));
 #pragma unroll
           for (int u = 0; u < 8; ++u) part[u] = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const int key = kbase + c;
-            const float s = (key <= limit && key < it.k_len)
-                                ? __uint_as_float(sr[c]) * p.qk_scale_log2
-                                : -INFINITY;
+            const float s = c < nv ? __uint_as_float(sr[c]) * p.qk_scale_log2 : -INFINITY;
             sr[c] = __float_as_uint(s);
             part[c & 7] = fmaxf(part[c & 7], s);
           }
@@ -507,11 +506,13 @@ __global__ void __launch_bounds__(kThreadsP, 2)
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
         } else {
+          // masked scores are -inf and 2^-inf = 0; a row with no unmasked key yet (m_run = -inf)
+          // has only masked scores here, so any finite offset gives its zeros
+          const float mm = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float s0 = __uint_as_float(sr[c]), s1 = __uint_as_float(sr[c + 1]);
-            const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
-            const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
+            const float p0 = fast_exp2(__uint_as_float(sr[c]) - mm);
+            const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - mm);
             part[(c >> 1) & 7] += p0 + p1;
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
