@@ -3,6 +3,8 @@
 Bars: the cache after kv_store is bit-exact; attention outputs are within max-abs 2e-2 of the
 oracle (N(0,1) inputs), and exactly bf16(V0) when the context is one token.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -123,6 +125,17 @@ def test_decode_shapes(orc, shape, q_scale):
                                 pad_slots=2, q_scale=q_scale)
     out, _ = _run_decode(case)
     assert_attn_close(out, _oracle_decode(orc, case), what=f"decode {shape}")
+
+
+@pytest.mark.parametrize("scale", [-0.0884, 0.0], ids=["negative", "zero"])
+def test_decode_scale_sign(orc, scale):
+    """Any scale is a valid input: a negative one flips which keys dominate, zero gives the mean
+    of the visible V rows. Split and unsplit decode both follow the oracle."""
+    for split in (0, 128):
+        case = dataclasses.replace(
+            W.random_decode_case(3030, 6, 32, 8, 128, 16, 1, 700, extra_pool=3), scale=scale)
+        out, _ = _run_decode(case, split_tokens=split)
+        assert_attn_close(out, _oracle_decode(orc, case), what=f"scale={scale} split={split}")
 
 
 def test_decode_ragged_edges(orc):

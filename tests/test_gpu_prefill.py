@@ -4,6 +4,8 @@ The new tokens are stored with kv_store first (as the engine does); the kernel t
 through the block table. The oracle reads the cached prefix through the table and the new keys from
 k/v directly, so the two share no step. Bar: max-abs error <= 2e-2 on N(0,1) inputs.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -82,6 +84,18 @@ def test_prefill_shared_prefix(orc, BS, q_scale):
                                  suffix_lens=np.array([1, 63, 64, 300]))
     out, _, _ = _run_paged(case)
     assert_attn_close(out, _oracle(orc, case), what=f"prefix BS={BS} q_scale={q_scale}")
+
+
+@pytest.mark.parametrize("scale", [-0.0884, 0.0, 0.25], ids=["negative", "zero", "large"])
+def test_prefill_scale_sign(orc, scale):
+    """Any scale is a valid input. With scale <= 0 every tile takes the masked path, which
+    scales before the max (the full-tile path takes the max of raw scores, correct only for a
+    positive scale). Scale 0 gives uniform weights over each row's visible keys."""
+    case = dataclasses.replace(
+        W.prefix_prefill_case(65, 3, 256, 1, 200, 32, 8, 128, 64,
+                              suffix_lens=np.array([1, 70, 200])), scale=scale)
+    out, _, _ = _run_paged(case)
+    assert_attn_close(out, _oracle(orc, case), what=f"scale={scale}")
 
 
 @pytest.mark.parametrize("Hq", [8, 16, 64], ids=["G1", "G2", "G8"])
