@@ -55,8 +55,9 @@ def source_digest(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key, source):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+def profiled(kernel_key, source):
+    """The committed ncu figures of one kernel launch (profiles/traffic.json), or None once the
+    kernel source has changed since they were captured."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -64,7 +65,25 @@ def profiled_traffic(kernel_key, source):
         d = json.load(f).get(kernel_key)
     if not d or d.get("source_sha") != source_digest(source):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d
+
+
+def profiled_traffic(kernel_key, source):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    d = profiled(kernel_key, source)
+    return None if d is None else d.get("dram_bytes_per_launch")
+
+
+PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_prefill.cu")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_decode.cu")
+
+
+def prefill_profile_keys():
+    """traffic and tensor-pipe utilisation of the prefix-prefill launch, from ncu (or None)."""
+    d = profiled("paged_prefill_prefix", PREFILL_SRC) or {}
+    return {"traffic": d.get("dram_bytes_per_launch"),
+            "tensor_pipe_active_pct": d.get("tensor_pipe_active_pct"),
+            "ncu_source_sha": d.get("source_sha")}
 
 
 class ClockSampler:
@@ -285,11 +304,7 @@ def prefill_arm(args, torch, pk, device):
             "data": "synthetic", "config": {"workload": "prefix_prefill", "num_seqs": 64,
                                             "new_tokens": ps.tokens, "prefix": 1024},
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tf / peak, "peak_source": kind,
-                         "traffic": profiled_traffic(
-                             "paged_prefill_prefix",
-                             os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc",
-                                          "paged_prefill.cu"))},
+                         "frac": tf / peak, "peak_source": kind, **prefill_profile_keys()},
             "device_error_flags": pk.get_device_error()}
     print(json.dumps(line), flush=True)
     return 0
@@ -462,9 +477,7 @@ def main():
     tokens_per_s = job_throughput(step.B, ms / 1e3, world)
     peak, peak_kind = measured_peaks()
     achieved = step.kv_bytes_per_layer / (decode_ms_mean / 1e3) / 1e9
-    traffic = profiled_traffic("paged_decode_qwen3_8b",
-                               os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc",
-                                            "paged_decode.cu"))
+    traffic = profiled_traffic("paged_decode_qwen3_8b", DECODE_SRC)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -651,7 +664,7 @@ def secondary_measurements(torch, pk, device, main_step):
         peak, _ = measured_tensor_peak()
         tf = ps.flops / (ms / 1e3) / 1e12
         res["prefix_prefill"] = {"ms": ms, "TFLOP/s": tf, "frac_of_bf16_peak": tf / peak,
-                                 "new_tokens": ps.tokens}
+                                 "new_tokens": ps.tokens, **prefill_profile_keys()}
         del ps
     except Exception as e:
         res["prefix_prefill"] = {"error": repr(e)}
@@ -660,15 +673,42 @@ def secondary_measurements(torch, pk, device, main_step):
     except Exception as e:
         res["mixed_prefill_decode"] = {"error": repr(e)}
     try:
-        layer = _decode_layer("qwen3_0p6b_decode", torch, device)
-        ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
-                                           layer["ctx"], layer["scale"], out=layer["out"],
-                                           plan=layer["plan"], workspace=layer["ws"]))
-        res["qwen3_0p6b_decode_layer"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6}
-        del layer
+        res["qwen3_0p6b_step"] = _qwen3_0p6b_step(torch, pk, device)
     except Exception as e:
-        res["qwen3_0p6b_decode_layer"] = {"error": repr(e)}
+        res["qwen3_0p6b_step"] = {"error": repr(e)}
     return res
+
+
+def _qwen3_0p6b_step(torch, pk, device, steps=10):
+    """The whole Qwen3-0.6B-shaped decode step: 28 layers x (kv_store of the newest token of 256
+    sequences, then paged decode), one distinct layer pool each (while memory allows), timed like
+    the headline step: CUDA events around the step and around every decode call."""
+    st = DecodeStep("qwen3_0p6b_decode", torch, pk, device, log_fill=False)
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(st.L)]
+           for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        st.run(evs[i])
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    dec = [e[0].elapsed_time(e[1]) for s_ in evs for e in s_]
+    dec_ms = sum(dec) / len(dec)
+    peak, _ = measured_peaks()
+    kv_step = st.kv_bytes_per_layer * st.L
+    achieved = st.kv_bytes_per_layer / (dec_ms / 1e3) / 1e9
+    out = {"ms_per_step": ms, "GB/s": kv_step / ms / 1e6,
+           "decode_tokens_per_s": st.B / (ms / 1e3), "frac_of_hbm_peak": kv_step / ms / 1e6 / peak,
+           "decode_mean_launch_ms": dec_ms, "decode_frac": achieved / peak,
+           "num_seqs": st.B, "num_layers": st.L, "distinct_layer_pools": st.n_pools,
+           "kv_bytes_per_step": kv_step, "flags": pk.get_device_error()}
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 def _mixed_batch(torch, pk, device, timed):

@@ -189,9 +189,12 @@ PKV_API int pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens
  *  - A plan whose workspace_bytes exceeds PKV_STATIC_WS_BYTES is rejected with
  *    PKV_ERR_WORKSPACE_TOO_SMALL (pkv_last_error() gives both sizes) before anything is enqueued;
  *    a plan with fewer splits (split_tokens_hint < 0 never splits) needs far less.
- *  - The first call on each device looks up the array's device address on that device; make
- *    that first call before any stream capture.
- *  - All calls on a device share the array, which keeps the previous call's contents; each call
+ *  - The array exists once per CUDA context (normally once per device, in its primary context).
+ *    The first call in a context looks up the array's device address with that context current
+ *    and keeps it under the driver's unique context id; make that first call before any stream
+ *    capture. A context the caller creates itself, or the device's new primary context after
+ *    cudaDeviceReset, has a new id and gets a fresh lookup, so no stale address is ever used.
+ *  - All calls in a context share the array, which keeps the previous call's contents; each call
  *    re-initialises what must start at zero itself. Calls that overlap on the GPU (unordered
  *    streams) race on the array: order them, e.g. on one stream.
  * The caller still owns and passes every input and the output.
@@ -266,8 +269,11 @@ PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16
                       void* stream);
 
 /*
- * Read and clear the device error word of the current device (PKV_DEVERR_* bits). Synchronises
- * the device first; not for use inside stream capture.
+ * Read and clear the device error word of the current CUDA context (PKV_DEVERR_* bits; one word
+ * per context, normally one per device). Synchronises the device first; not for use inside stream
+ * capture. The library keeps its per-context state (this word's address, kernel attributes) under
+ * the driver's unique context id, so a context created by the caller, or the primary context that
+ * replaces one destroyed by cudaDeviceReset, gets its own.
  */
 PKV_API int pkv_get_device_error(int32_t* flags);
 

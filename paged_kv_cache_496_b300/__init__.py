@@ -165,13 +165,28 @@ _ws_lock = threading.Lock()
 _ws_cache: dict = {}
 
 
-def workspace_for(plan: DecodePlan, device: torch.device) -> torch.Tensor:
-    """A grow-only per-device workspace (uint8, 256-byte aligned by the caching allocator)."""
-    key = torch.device(device).index
+def _key_and_stream(device, stream):
+    dev = torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    return (dev.index, s.cuda_stream), s
+
+
+def workspace_for(plan: DecodePlan, device: torch.device, stream=None) -> torch.Tensor:
+    """The default decode workspace of (device, stream): grow-only, uint8, 256-byte aligned by the
+    caching allocator.
+
+    Calls on one stream run in order, so they share it; calls on different streams get different
+    workspaces and never race. The buffer is allocated on `stream` itself, so when it is replaced
+    by a larger one the caching allocator hands its memory out again only to work on that stream,
+    i.e. after the kernels that used it.
+    """
+    key, s = _key_and_stream(device, stream)
     with _ws_lock:
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < plan.workspace_bytes:
-            ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+            with torch.cuda.stream(s):
+                ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8,
+                                 device=key[0])
             _ws_cache[key] = ws
         return ws
 
@@ -205,7 +220,7 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
             max_context_len = int(context_lens.max().item()) if B else 0
         plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens)
     if workspace is None:
-        workspace = workspace_for(plan, q.device)
+        workspace = workspace_for(plan, q.device, stream)
     _check(lib.pkv_paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                 _cache_desc(k_cache), block_tables.data_ptr(),
                                 block_tables.shape[1], context_lens.data_ptr(), B, Hq,
@@ -239,7 +254,7 @@ def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_ta
             max_context_len = int(context_lens.max().item()) if B else 0
         plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens)
     if workspace is None:
-        workspace = workspace_for(plan, q.device)
+        workspace = workspace_for(plan, q.device, stream)
     _check(lib.pkv_paged_decode_store(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                                       slot_mapping.data_ptr(), k_cache.data_ptr(),
                                       v_cache.data_ptr(), _cache_desc(k_cache),
@@ -254,14 +269,15 @@ PREFILL_WORKSPACE_BYTES = 256  # PKV_PREFILL_WORKSPACE_BYTES
 _prefill_ws: dict = {}
 
 
-def prefill_workspace(device: torch.device) -> torch.Tensor:
-    """The per-device default prefill workspace (a work counter). Calls that may overlap on
-    different streams should each pass their own workspace."""
-    key = torch.device(device).index
+def prefill_workspace(device: torch.device, stream=None) -> torch.Tensor:
+    """The default prefill workspace (a work counter) of (device, stream), allocated on that
+    stream: calls on one stream share it in order, calls on different streams never race."""
+    key, s = _key_and_stream(device, stream)
     with _ws_lock:
         ws = _prefill_ws.get(key)
         if ws is None:
-            ws = torch.empty(PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+            with torch.cuda.stream(s):
+                ws = torch.empty(PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=key[0])
             _prefill_ws[key] = ws
         return ws
 
@@ -294,7 +310,7 @@ def paged_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, block_tables, scale: floa
     if max_seqlen_q is None:
         max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
     if workspace is None:
-        workspace = prefill_workspace(q.device)
+        workspace = prefill_workspace(q.device, stream)
     _check(lib.pkv_paged_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                  cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Tq,
                                  int(max_seqlen_q), bt_ptr, mb, kc_ptr, vc_ptr, desc, Hq,

@@ -1,13 +1,14 @@
 // abi.cu -- the extern "C" entry points of libpagedkv.so (declared in include/pagedkv.h).
 //
-// Host-side argument validation, TMA descriptor encoding, the per-device error word and status
-// strings. Every entry point only enqueues work on the caller's stream; nothing here allocates
+// Host-side argument validation, TMA descriptor encoding, the per-context library state (device
+// error word, kernel attributes) and status strings. Every entry point only enqueues work on the caller's stream; nothing here allocates
 // device memory.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -29,63 +30,116 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-// Device error word: one per device (each device has its own copy of a __device__ variable).
+// Device error word: one copy per CUDA context (a __device__ variable exists once per loaded
+// module, and each context loads its own).
 __device__ int g_device_flags = 0;
 
-constexpr int kMaxDevices = 64;
-struct DeviceInfo {
-  bool ready = false;
-  int* flags = nullptr;
-  int num_sms = 0;
-};
-DeviceInfo g_devices[kMaxDevices];
-std::mutex g_device_mutex;
-
-int device_info(DeviceInfo* out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device index %d", dev);
-  std::lock_guard<std::mutex> lock(g_device_mutex);
-  DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_flags);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    d.flags = static_cast<int*>(p);
-    d.num_sms = sms;
-    d.ready = true;
-  }
-  *out = d;
-  return PKV_OK;
-}
-
-// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no link to libcuda).
+// Driver entry points, fetched through the runtime (no link to libcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct DriverFns {
+  EncodeTiledFn encode = nullptr;
+  CtxGetCurrentFn ctx_get_current = nullptr;
+  CtxGetIdFn ctx_get_id = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+
+const DriverFns& driver_fns() {
+  static std::once_flag once;
+  static DriverFns fns;
+  std::call_once(once, [] {
+    auto get = [](const char* name) -> void* {
+      void* f = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      const cudaError_t e = cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
+        if (fns.err == cudaSuccess) fns.err = e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+        return nullptr;
+      }
+      return f;
+    };
+    fns.encode = reinterpret_cast<EncodeTiledFn>(get("cuTensorMapEncodeTiled"));
+    fns.ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(get("cuCtxGetCurrent"));
+    fns.ctx_get_id = reinterpret_cast<CtxGetIdFn>(get("cuCtxGetId"));
+  });
+  return fns;
+}
 
 int get_encoder(EncodeTiledFn* fn) {
-  static std::once_flag once;
-  static EncodeTiledFn encoder = nullptr;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                           &q);
-    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess)
-      encoder = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  if (encoder == nullptr)
-    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(err));
-  *fn = encoder;
+  const DriverFns& f = driver_fns();
+  if (f.encode == nullptr)
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(f.err));
+  *fn = f.encode;
   return PKV_OK;
 }
+
+// One entry per context this process has used; entries are never freed (there are only a few).
+std::mutex g_context_mutex;
+std::vector<ContextState*> g_contexts;
+
+}  // namespace
+
+int report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+int current_context_id(unsigned long long* id, int* device) {
+  const DriverFns& f = driver_fns();
+  if (f.ctx_get_current == nullptr || f.ctx_get_id == nullptr)
+    return fail(PKV_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId unavailable (%s)",
+                cudaGetErrorName(f.err));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  CUcontext c = nullptr;
+  if (f.ctx_get_current(&c) != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (c == nullptr) {
+    // nothing bound to this thread yet: cudaSetDevice initialises and binds the primary context
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    if (f.ctx_get_current(&c) != CUDA_SUCCESS || c == nullptr)
+      return fail(PKV_ERR_CUDA, "no CUDA context is current");
+  }
+  unsigned long long v = 0;
+  if (f.ctx_get_id(c, &v) != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuCtxGetId failed");
+  *id = v;
+  if (device != nullptr) *device = dev;
+  return PKV_OK;
+}
+
+int context_state(const ContextState** out) {
+  unsigned long long id = 0;
+  int dev = 0;
+  int st = current_context_id(&id, &dev);
+  if (st != PKV_OK) return st;
+  std::lock_guard<std::mutex> lock(g_context_mutex);
+  for (const ContextState* s : g_contexts)
+    if (s->ctx_id == id) {
+      *out = s;
+      return PKV_OK;
+    }
+  ContextState s;
+  s.ctx_id = id;
+  s.device = dev;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_device_flags);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+  s.flags = static_cast<int*>(p);
+  e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  e = configure_prefill_kernel();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill kernel attributes");
+  e = configure_decode_kernels(s.decode_ctas);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel attributes");
+  g_contexts.push_back(new ContextState(s));
+  *out = g_contexts.back();
+  return PKV_OK;
+}
+
+namespace {
 
 // 3-D view {D, heads, rows} of a row-major [rows, heads, D] bf16 tensor;
 // box {box_d, box_heads, box_rows}.
@@ -172,16 +226,16 @@ const char* pkv_status_string(int status) {
 
 int pkv_get_device_error(int32_t* flags) {
   if (flags == nullptr) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
-  DeviceInfo d;
-  int st = device_info(&d);
+  const ContextState* d = nullptr;
+  int st = context_state(&d);
   if (st != PKV_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   int v = 0;
-  e = cudaMemcpy(&v, d.flags, sizeof v, cudaMemcpyDeviceToHost);
+  e = cudaMemcpy(&v, d->flags, sizeof v, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
   const int zero = 0;
-  e = cudaMemcpy(d.flags, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  e = cudaMemcpy(d->flags, &zero, sizeof zero, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
   *flags = v;
   return PKV_OK;
@@ -189,10 +243,10 @@ int pkv_get_device_error(int32_t* flags) {
 
 int pkv_selftest_bounded_wait(void* stream) {
   g_last_error[0] = 0;
-  DeviceInfo d;
-  int st = device_info(&d);
+  const ContextState* d = nullptr;
+  int st = context_state(&d);
   if (st != PKV_OK) return st;
-  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d.flags);
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d->flags);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return PKV_OK;
@@ -210,11 +264,11 @@ int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* slot_mappi
     return fail(PKV_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
-  DeviceInfo d;
-  st = device_info(&d);
+  const ContextState* d = nullptr;
+  st = context_state(&d);
   if (st != PKV_OK) return st;
   cudaError_t e = launch_kv_store(k, v, slot_mapping, num_tokens, k_cache, v_cache, cache,
-                                  d.num_sms, d.flags, static_cast<cudaStream_t>(stream));
+                                  d->num_sms, d->flags, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_store launch");
   return PKV_OK;
 }
@@ -231,11 +285,11 @@ int block_move(int mode, uint16_t* k_cache, uint16_t* v_cache, const pkv_cache_d
   if (!aligned16(k_cache) || !aligned16(v_cache) ||
       (mode != 0 && (!aligned16(buf_k) || !aligned16(buf_v))))
     return fail(PKV_ERR_INVALID_ARG, "caches and buffers must be 16-byte aligned");
-  DeviceInfo d;
-  st = device_info(&d);
+  const ContextState* d = nullptr;
+  st = context_state(&d);
   if (st != PKV_OK) return st;
   cudaError_t e = launch_block_move(mode, k_cache, v_cache, ids, n, cache, buf_k, buf_v,
-                                    d.num_sms, d.flags, static_cast<cudaStream_t>(stream));
+                                    d->num_sms, d->flags, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "block move launch");
   return PKV_OK;
 }
@@ -268,11 +322,11 @@ int pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens, int32_
     return fail(PKV_ERR_UNSUPPORTED, "block_size %d (must be even, 2..256)", block_size);
   if (num_seqs == 0 || max_blocks == 0) return PKV_OK;
   if (!token_ids || !cu_seqlens || !out) return fail(PKV_ERR_INVALID_ARG, "null pointer");
-  DeviceInfo d;
-  int st = device_info(&d);
+  const ContextState* d = nullptr;
+  int st = context_state(&d);
   if (st != PKV_OK) return st;
   cudaError_t e = launch_block_hashes(token_ids, cu_seqlens, num_seqs, block_size, max_blocks,
-                                      out, d.flags, static_cast<cudaStream_t>(stream));
+                                      out, d->flags, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "block hash launch");
   return PKV_OK;
 }
@@ -346,8 +400,8 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
   if (workspace_bytes < need)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, plan needs %zu",
                 workspace_bytes, need);
-  DeviceInfo d;
-  st = device_info(&d);
+  const ContextState* d = nullptr;
+  st = context_state(&d);
   if (st != PKV_OK) return st;
   const int box_t = decode_box_rows(cache.head_dim, num_q_heads / cache.num_kv_heads,
                                     cache.block_size);
@@ -373,11 +427,12 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
   a.max_splits = plan->max_splits;
   a.auto_split = plan->auto_split != 0;
   a.out = out;
-  a.flags = d.flags;
+  a.flags = d->flags;
   a.k_new = k_new;
   a.v_new = v_new;
   a.slot_mapping = slot_mapping;
-  cudaError_t e = launch_paged_decode(a, tk, tv, d.num_sms, static_cast<cudaStream_t>(stream));
+  a.ctas_per_sm = d->decode_ctas;
+  cudaError_t e = launch_paged_decode(a, tk, tv, d->num_sms, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return fail(PKV_ERR_UNSUPPORTED, "no decode instance");
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;
@@ -449,8 +504,8 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   }
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
     return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
-  DeviceInfo d;
-  st = device_info(&d);
+  const ContextState* d = nullptr;
+  st = context_state(&d);
   if (st != PKV_OK) return st;
   const int G = num_q_heads / cache.num_kv_heads;
   CUtensorMap tq, tk, tv;
@@ -488,9 +543,9 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   a.num_q_heads = num_q_heads;
   a.scale = scale;
   a.out = out;
-  a.flags = d.flags;
+  a.flags = d->flags;
   a.item_counter = static_cast<int32_t*>(workspace);
-  cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d.num_sms,
+  cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d->num_sms,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
   return PKV_OK;

@@ -15,35 +15,45 @@
 // cleared here. Two calls that overlap on the GPU (different streams, no ordering between them)
 // race on the array and corrupt each other's results: order them, for example on one stream.
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_static_workspace[PKV_STATIC_WS_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_workspace_addr[kMaxDevices] = {};
+// Device address of the array in each CUDA context seen so far, keyed by the driver's unique
+// context id. Host code cannot use the symbol itself (it names a host-side stand-in), and each
+// context (normally one per device: its primary context) holds its own copy of the array, so the
+// first call in a context looks the address up with that context current and keeps it. After
+// cudaDeviceReset the device's new primary context has a new id and gets a fresh lookup.
+struct WorkspaceAddr {
+  unsigned long long ctx_id;
+  void* addr;
+};
 std::mutex g_workspace_mutex;
+std::vector<WorkspaceAddr> g_workspace_addrs;
 
-// Device address of the current device's copy of the array. Host code cannot use the symbol
-// itself (it names a host-side stand-in), so the first call on each device looks the address up
-// with that device current and keeps it.
-cudaError_t static_workspace(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+int static_workspace(void** out) {
+  unsigned long long id = 0;
+  int st = pkv::current_context_id(&id, nullptr);
+  if (st != PKV_OK) return st;
   std::lock_guard<std::mutex> lock(g_workspace_mutex);
-  if (g_workspace_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_workspace);
-    if (e != cudaSuccess) return e;
-    if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_workspace_addr[dev] = p;
-  }
-  *out = g_workspace_addr[dev];
-  return cudaSuccess;
+  for (const WorkspaceAddr& w : g_workspace_addrs)
+    if (w.ctx_id == id) {
+      *out = w.addr;
+      return PKV_OK;
+    }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+  if (e != cudaSuccess) return pkv::report_cuda_error(e, "cudaGetSymbolAddress(static workspace)");
+  if (p == nullptr)
+    return pkv::report_cuda_error(cudaErrorInvalidSymbol, "cudaGetSymbolAddress(static workspace)");
+  g_workspace_addrs.push_back(WorkspaceAddr{id, p});
+  *out = p;
+  return PKV_OK;
 }
 
 }  // namespace
@@ -54,7 +64,8 @@ extern "C" PKV_API int pkv_paged_decode_static_ws(
     int32_t num_seqs, int32_t num_q_heads, float scale, const pkv_decode_plan* plan,
     uint16_t* out, void* stream) {
   void* ws = nullptr;
-  if (static_workspace(&ws) != cudaSuccess) return PKV_ERR_CUDA;
+  const int st = static_workspace(&ws);
+  if (st != PKV_OK) return st;
   // pkv_paged_decode validates every argument and rejects a plan whose workspace exceeds
   // PKV_STATIC_WS_BYTES (PKV_ERR_WORKSPACE_TOO_SMALL, with both sizes in pkv_last_error())
   // before anything is enqueued.

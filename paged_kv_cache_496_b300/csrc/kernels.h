@@ -13,6 +13,38 @@ namespace pkv {
 // of the largest tile (128 tokens).
 constexpr int kSplitQuantum = 128;
 
+// Decode kernel instances: head_dim {128, 64} x query heads per CTA {4, 2, 1} x {plain, fused}.
+constexpr int kDecodeInstances = 12;
+
+// State of the library in one CUDA context. Module globals (the device error word, the static
+// decode workspace) and kernel attributes exist once per context, so they are looked up or set
+// once per context and kept under the driver's unique context id: a context the caller created
+// itself, or the new primary context after cudaDeviceReset, gets an entry of its own.
+struct ContextState {
+  unsigned long long ctx_id = 0;
+  int device = 0;
+  int num_sms = 0;
+  int* flags = nullptr;                   // this context's copy of the device error word
+  int decode_ctas[kDecodeInstances] = {};  // resident CTAs per SM of each decode instance
+};
+
+// The calling thread's current context (its primary context is bound first if none is). The
+// first call in a context sets it up: symbol lookups, shared-memory opt-ins, occupancy queries.
+// Returns PKV_OK or a PKV_ERR_* status with the message in pkv_last_error().
+int context_state(const ContextState** out);
+
+// Unique id of the calling thread's current context (binding the device's primary context if
+// none is current yet). Returns PKV_OK or a PKV_ERR_* status.
+int current_context_id(unsigned long long* id, int* device);
+
+// Records "what: <CUDA error>" as the message pkv_last_error() returns; returns PKV_ERR_CUDA.
+int report_cuda_error(cudaError_t e, const char* what);
+
+// One-time attributes of the attention kernels in the current context (shared-memory opt-in,
+// carve-out); the decode call also reports each instance's resident CTAs per SM.
+cudaError_t configure_decode_kernels(int (&ctas_per_sm)[kDecodeInstances]);
+cudaError_t configure_prefill_kernel();
+
 struct DecodeWorkspace {
   uint32_t* header;    // [0] claim counter, [1] number of items, [2] chunk length (tokens)
   int2* items;         // (sequence, chunk) pairs, B * max_splits entries at most
@@ -50,6 +82,7 @@ struct DecodeArgs {
   const uint16_t* k_new = nullptr;
   const uint16_t* v_new = nullptr;
   const int32_t* slot_mapping = nullptr;
+  const int* ctas_per_sm = nullptr;  // ContextState::decode_ctas of the current context
 };
 
 // Whole-block moves: mode 0 copies (src, dst) pairs inside the caches, mode 1 gathers blocks

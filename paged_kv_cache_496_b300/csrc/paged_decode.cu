@@ -897,18 +897,18 @@ cudaError_t configure_instance(int* ctas_per_sm) {
   return cudaSuccess;
 }
 
+// Index of an instance in ContextState::decode_ctas.
+constexpr int decode_instance(int D, int GH, bool fuse) {
+  return (D == 128 ? 0 : 6) + (GH == 4 ? 0 : GH == 2 ? 2 : 4) + (fuse ? 1 : 0);
+}
+
 template <int D, int GH>
 cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int num_sms, cudaStream_t stream) {
   using T = Traits<D, GH>;
   const bool fuse = a.k_new != nullptr;
-  static int ctas_plain = 0, ctas_fused = 0;  // per process; all B300s alike
-  int& ctas_per_sm = fuse ? ctas_fused : ctas_plain;
-  if (ctas_per_sm == 0) {
-    const cudaError_t e = fuse ? configure_instance<D, GH, true>(&ctas_per_sm)
-                               : configure_instance<D, GH, false>(&ctas_per_sm);
-    if (e != cudaSuccess) return e;
-  }
+  const int ctas_per_sm = a.ctas_per_sm[decode_instance(D, GH, fuse)];
+  if (ctas_per_sm <= 0) return cudaErrorInvalidConfiguration;
   const int G = a.num_q_heads / a.cache.num_kv_heads;
   DecodeParams p;
   p.q = a.q;
@@ -1001,6 +1001,22 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t hea
     carve->part_ml = max_splits > 1 ? reinterpret_cast<float2*>(b8 + ml) : nullptr;
   }
   return off;
+}
+
+cudaError_t configure_decode_kernels(int (&ctas)[kDecodeInstances]) {
+  cudaError_t e = cudaSuccess;
+#define PKV_CONFIGURE(D, GH)                                                                     \
+  if (e == cudaSuccess)                                                                          \
+    e = configure_instance<D, GH, false>(&ctas[decode_instance(D, GH, false)]);                 \
+  if (e == cudaSuccess) e = configure_instance<D, GH, true>(&ctas[decode_instance(D, GH, true)]);
+  PKV_CONFIGURE(128, 4)
+  PKV_CONFIGURE(128, 2)
+  PKV_CONFIGURE(128, 1)
+  PKV_CONFIGURE(64, 4)
+  PKV_CONFIGURE(64, 2)
+  PKV_CONFIGURE(64, 1)
+#undef PKV_CONFIGURE
+  return e;
 }
 
 int decode_box_rows(int head_dim, int group, int block_size) {

@@ -606,6 +606,14 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 
 int prefill_positions_per_tile(int group) { return kRows / group; }
 
+cudaError_t configure_prefill_kernel() {
+  cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 int prefill_kv_box_rows(int block_size, bool paged) {
   return paged ? (block_size < kKeys ? block_size : kKeys) : kKeys;
 }
@@ -613,16 +621,6 @@ int prefill_kv_box_rows(int block_size, bool paged) {
 cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
                                  const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
                                  cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   const int G = a.num_q_heads / a.cache.num_kv_heads;
   PrefillParams p;
   p.cu_q = a.cu_seqlens_q;

@@ -146,14 +146,43 @@ def test_prefill_bad_block_flagged_not_faulted():
     assert pk.get_device_error() & pk.DEVERR_BAD_BLOCK
 
 
+def _head_subcase(case: W.PrefillCase, seqs, g: int) -> W.PrefillCase:
+    """The sub-problem of sequences `seqs` restricted to kv head g and its G query heads (heads are
+    independent, so this is the same attention on fewer heads)."""
+    G = case.num_q_heads // case.num_kv_heads
+    rows = np.concatenate([np.arange(case.cu_seqlens_q[b], case.cu_seqlens_q[b + 1])
+                           for b in seqs]).astype(np.int64)
+    ql, kl = case.q_lens[seqs], case.k_lens[seqs]
+    return W.PrefillCase(
+        case.num_blocks, case.block_size, 1, case.head_dim, G,
+        np.ascontiguousarray(case.k_cache[:, :, g:g + 1]),
+        np.ascontiguousarray(case.v_cache[:, :, g:g + 1]),
+        np.ascontiguousarray(case.q[rows, g * G:(g + 1) * G]),
+        np.ascontiguousarray(case.k[rows, g:g + 1]), np.ascontiguousarray(case.v[rows, g:g + 1]),
+        np.concatenate([[0], np.cumsum(ql)]).astype(np.int32),
+        np.concatenate([[0], np.cumsum(kl)]).astype(np.int32),
+        np.ascontiguousarray(case.block_tables[seqs]), case.slot_mapping[:0], case.scale)
+
+
 @pytest.mark.slow
 def test_full_prefix_prefill_workload(orc):
     """64 sequences sharing a 1024-token prefix (4 blocks of 256), U{100..1024} new tokens each,
-    in the launch configuration the benchmark times; sampled sequences against the oracle."""
+    in the launch configuration the benchmark times. Every sequence is compared with the oracle
+    on one kv head (all G query heads of it; sequence b on kv head b % 8, so every head and every
+    item ordering of the persistent grid is covered), and three sequences (longest, shortest,
+    index 17) on all heads."""
     ql = W.prefix_prefill_suffix_lengths()
     case = W.prefix_prefill_case(4, 64, 1024, 100, 1024, 32, 8, 128, 256, suffix_lens=ql)
     out, _, _ = _run_paged(case)
     assert torch.isfinite(out.float()).all()
+    G = case.num_q_heads // case.num_kv_heads
+    for g in range(case.num_kv_heads):
+        seqs = np.arange(g, case.num_seqs, case.num_kv_heads)
+        ref = _oracle(orc, _head_subcase(case, seqs, g))
+        rows = np.concatenate([np.arange(case.cu_seqlens_q[b], case.cu_seqlens_q[b + 1])
+                               for b in seqs])
+        got = out[torch.as_tensor(rows, device=out.device), g * G:(g + 1) * G]
+        assert_attn_close(got, ref, what=f"full workload kv head {g}, sequences {list(seqs)}")
     for b in (int(np.argmax(ql)), int(np.argmin(ql)), 17):
         sub = W.PrefillCase(case.num_blocks, 256, 8, 128, 32, case.k_cache, case.v_cache,
                             case.q[case.cu_seqlens_q[b]:case.cu_seqlens_q[b + 1]],
