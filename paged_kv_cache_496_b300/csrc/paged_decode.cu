@@ -401,9 +401,11 @@ __global__ void __maxnreg__(168)
     const uint32_t total = p.header[1] * (uint32_t)p.head_groups;
     const int split = (int)p.header[2];
     const int bs = p.block_size;
+    // block_size is a power of two: shifts and masks instead of divisions by a runtime value
+    const int lbs = __ffs(bs) - 1;
     const int box_t = bs < T::kTileT ? bs : T::kTileT;
     const int nsub = T::kTileT / box_t;
-    const int ent_per_tile = (T::kTileT + bs - 1) / bs;
+    const int ent_per_tile = (T::kTileT + bs - 1) >> lbs;
     uint32_t issue = 0;
     bool ok = true;
     // Block-table window: entries [win_base, win_base + 32) of sequence win_b, one per lane, and
@@ -457,7 +459,7 @@ __global__ void __maxnreg__(168)
       const int nsplit = (ctx + split - 1) / split;
       const int tok_begin = s * split;
       const int tok_end = min(ctx, tok_begin + split);
-      const int need_ent = (ctx + bs - 1) / bs;  // table entries of the whole sequence
+      const int need_ent = (ctx + bs - 1) >> lbs;  // table entries of the whole sequence
       const int32_t* bt_row = p.block_tables + (int64_t)b * p.max_blocks;
       const uint16_t* qsrc = p.q + ((int64_t)b * p.num_q_heads + x * GH) * D;
       const int kv_head = x / p.groups_per_kv;
@@ -482,9 +484,10 @@ __global__ void __maxnreg__(168)
           }
           if (lane == 0 && slot != -1) {
             const int pos = ctx - 1;
-            const int e = pos / bs;
+            const int e = pos >> lbs;
             const int blk = e < p.max_blocks ? __ldg(bt_row + e) : -1;
-            if (!writes || slot != blk * bs + pos % bs) raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
+            if (!writes || slot != blk * bs + (pos & (bs - 1)))
+              raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
           }
           __syncwarp();
           fence_proxy_async_global();  // lane 0 issues the copies that read the row
@@ -493,7 +496,7 @@ __global__ void __maxnreg__(168)
 
       for (int tok0 = tok_begin; tok0 < tok_end && ok; tok0 += T::kTileT) {
         const int st = issue % T::kStages;
-        const int e0 = tok0 / bs;
+        const int e0 = tok0 >> lbs;
         if (win_b != b || e0 < win_base || e0 + ent_per_tile > win_base + 32) {
           if (win_b == b && e0 >= win_base + 32 && e0 + ent_per_tile <= win_base + 64) {
             win_base += 32;  // step into the prefetched window
@@ -514,7 +517,7 @@ __global__ void __maxnreg__(168)
           rows[sb] = -1;
           if (sb < nsub) {
             const int t = tok0 + sb * box_t;
-            const int blk = __shfl_sync(kFullMask, win_val, (t / bs - win_base) & 31);
+            const int blk = __shfl_sync(kFullMask, win_val, ((t >> lbs) - win_base) & 31);
             if (t < tok_end) {
               if (blk >= 0 && blk < p.num_blocks) {
                 rows[sb] = blk * bs + (t & (bs - 1));

@@ -65,8 +65,10 @@ constexpr int kBarFullK = 0, kBarEmptyK = kBarFullK + kKStages,
               kBarMma = kBarOFree + 1, kBarItemFull = kBarMma + 1, kBarItemEmpty = kBarItemFull + 2,
               kNumBars = kBarItemEmpty + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr int kOffItem = kOffTmemSlot + 16;  // int[2]: claimed item ids, -1 = no more work
-constexpr int kSmemBytes = kOffItem + 16;
+// Two item slots of kItemInts ints: the claimed id (-1 = no more work) and the item's fields
+constexpr int kItemInts = 12;
+constexpr int kOffItem = kOffTmemSlot + 16;
+constexpr int kSmemBytes = kOffItem + 2 * kItemInts * 4;
 constexpr int kItemReaders = 5;  // the MMA thread and the four softmax warps
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 && kKTile % 1024 == 0,
               "swizzle atoms need 1024-byte alignment");
@@ -103,6 +105,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 struct Item {
   int b, g, q_start, q_len, k_len, q0, P, n_kt;
 };
+static_assert(sizeof(Item) / 4 + 1 <= kItemInts, "item slot size");
 
 // Items are numbered so that the query tiles of one (sequence, kv head) are adjacent, longest
 // first: CTAs that run at the same time then share that head's K/V through L2. Returns false for
@@ -179,18 +182,38 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + kOffItem);
-  // consumers: the id of the n-th item this CTA works on (-1: none left, or a timeout)
-  auto next_item = [&](int n) -> int {
+  // The producer decodes each claimed item once and passes its fields to the other warps through
+  // a two-slot ring in shared memory, so that no consumer reloads the sequence lengths from
+  // global memory when it moves to the next item.
+  volatile int* item_slots = reinterpret_cast<volatile int*>(smem + kOffItem);
+  auto read_slot = [&](int n, Item& it) -> int {
+    volatile int* sl = item_slots + (n & 1) * kItemInts;
+    it.b = sl[1]; it.g = sl[2]; it.q_start = sl[3]; it.q_len = sl[4];
+    it.k_len = sl[5]; it.q0 = sl[6]; it.P = sl[7]; it.n_kt = sl[8];
+    return sl[0];
+  };
+  // one consumer thread: the id of the n-th item this CTA works on (-1: none left, or a timeout)
+  auto take_item_thread = [&](int n, Item& it) -> int {
     int id = -1;
-    if (lane == 0) {
-      if (mbar_wait(bar(kBarItemFull + (n & 1)), (n >> 1) & 1)) {
-        id = item_slot[n & 1];
-      } else {
-        raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
-      }
-      mbar_arrive(bar(kBarItemEmpty + (n & 1)));
+    if (mbar_wait(bar(kBarItemFull + (n & 1)), (n >> 1) & 1)) {
+      id = read_slot(n, it);
+    } else {
+      raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
     }
+    mbar_arrive(bar(kBarItemEmpty + (n & 1)));
+    return id;
+  };
+  // a whole consumer warp: lane 0 waits, every lane reads the slot, then lane 0 releases it
+  auto take_item_warp = [&](int n, Item& it) -> int {
+    int full = 0;
+    if (lane == 0) {
+      full = mbar_wait(bar(kBarItemFull + (n & 1)), (n >> 1) & 1) ? 1 : 0;
+      if (!full) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+    }
+    full = __shfl_sync(kFullMask, full, 0);
+    const int id = full ? read_slot(n, it) : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarItemEmpty + (n & 1)));
     return id;
   };
 
@@ -207,7 +230,11 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       tma_prefetch_desc(&tmap_v);
     }
     const bool paged = p.block_tables != nullptr;
+    // block_size is a power of two: positions map to table entries by shifts and masks (a
+    // division by a runtime value would cost the producer tens of instructions per tile)
     const int bs = p.block_size;
+    const int lbs = __ffs(bs) - 1;
+    const int ent = (kKeys + bs - 1) >> lbs;  // table entries one key tile spans
     const int box = p.box_rows;
     const int nsub = kKeys / box;
     int t = 0, n = 0, kr = 0;
@@ -262,18 +289,30 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         }
         ok = mbar_wait(bar(kBarItemEmpty + (n & 1)), ((n >> 1) & 1) ^ 1);
         if (ok) {
-          item_slot[n & 1] = id;
+          volatile int* sl = item_slots + (n & 1) * kItemInts;
+          sl[0] = id;
+          if (id >= 0) {
+            sl[1] = it.b; sl[2] = it.g; sl[3] = it.q_start; sl[4] = it.q_len;
+            sl[5] = it.k_len; sl[6] = it.q0; sl[7] = it.P; sl[8] = it.n_kt;
+          }
           mbar_arrive(bar(kBarItemFull + (n & 1)));
         }
       }
       ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
       id = __shfl_sync(kFullMask, id, 0);
       if (!ok || id < 0) break;
-      load_item(p, id, it);
+      it.b = __shfl_sync(kFullMask, it.b, 0);
+      it.g = __shfl_sync(kFullMask, it.g, 0);
+      it.q_start = __shfl_sync(kFullMask, it.q_start, 0);
+      it.q_len = __shfl_sync(kFullMask, it.q_len, 0);
+      it.k_len = __shfl_sync(kFullMask, it.k_len, 0);
+      it.q0 = __shfl_sync(kFullMask, it.q0, 0);
+      it.P = __shfl_sync(kFullMask, it.P, 0);
+      it.n_kt = __shfl_sync(kFullMask, it.n_kt, 0);
       int need_ent = 0;
       const int32_t* bt_row = nullptr;
       if (paged) {
-        need_ent = (it.k_len + bs - 1) / bs;
+        need_ent = (it.k_len + bs - 1) >> lbs;
         if (need_ent > p.max_blocks) {
           if (lane == 0) raise_flag(p.flags, PKV_DEVERR_CTX_CLAMPED);
           need_ent = p.max_blocks;
@@ -301,8 +340,7 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         for (int sb = 0; sb < kKeys / 16; ++sb) rows[sb] = p.oob_row;
         const int key0 = j * kKeys;
         if (paged) {
-          const int e0 = key0 / bs;
-          const int ent = (kKeys + bs - 1) / bs;
+          const int e0 = key0 >> lbs;
           if (e0 < win_base || e0 + ent > win_base + 32) {
             win_base = e0;
             const int e = e0 + lane;
@@ -312,8 +350,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           for (int sb = 0; sb < kKeys / 16; ++sb) {
             if (sb < nsub) {
               const int key = key0 + sb * box;
-              const int blk = __shfl_sync(kFullMask, win_val, (key / bs - win_base) & 31);
-              if (key < it.k_len && key / bs < need_ent) {
+              const int blk = __shfl_sync(kFullMask, win_val, ((key >> lbs) - win_base) & 31);
+              if (key < it.k_len && (key >> lbs) < need_ent) {
                 if (blk >= 0 && blk < p.num_blocks) {
                   rows[sb] = blk * bs + (key & (bs - 1));
                 } else if (lane == 0) {
@@ -327,18 +365,19 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           for (int sb = 0; sb < kKeys / 16; ++sb)
             if (sb < nsub) rows[sb] = it.q_start + key0 + sb * box;
         }
-        if (lane < kKStages + kVStages) ok = issue_kv(rows, it.g, true, t - 1, t > 0);
+        if (lane < kKStages + kVStages) ok = issue_kv(rows, it.g, true, t - 1, j > 0);
         ++kr;
         ok = __all_sync(kFullMask, ok);
 #pragma unroll
         for (int sb = 0; sb < kKeys / 16; ++sb) prev_rows[sb] = rows[sb];
         prev_g = it.g;
       }
+      // V of the item's last key tile goes out now, so that the item's last P V (issued as soon
+      // as its P is ready) does not wait for the next item's claim and Q
+      if (ok && lane < kKStages + kVStages) ok = issue_kv(prev_rows, prev_g, false, t - 1, true);
+      ok = __all_sync(kFullMask, ok);
       ++n;
     }
-    bool v_ok = true;  // V of the last key tile
-    if (ok && t > 0) v_ok = issue_kv(prev_rows, prev_g, false, t - 1, true);
-    ok = __all_sync(kFullMask, ok && v_ok);
     if (lane == 0) {
       if (!ok) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
       // never leave while a copy into this CTA's shared memory may be in flight: wait for the
@@ -387,10 +426,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       bool pending = false, pend_first = false;
       int pend_n = 0;
       while (ok) {
-        const int id = next_item(n);
-        if (id < 0) break;
         Item it;
-        load_item(p, id, it);
+        if (take_item_thread(n, it) < 0) break;
         // the previous item's S MMAs read Q's TMEM columns: they are complete before the copy
         // below overwrites them (an MMA followed by a copy is not ordered by the tensor core)
         if (ok && t > 0) ok = mbar_wait(bar(kBarSFull), (t - 1) & 1);
@@ -424,6 +461,11 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           pend_first = j == 0;
           pend_n = n;
         }
+        // The item's last P V goes out as soon as its P is ready, ahead of the next item's Q
+        // copy and first S: the softmax warps can then write out O while the next item's Q and
+        // first K tile are still arriving.
+        if (pending) issue_pv(t - 1, pend_first, pend_n);
+        pending = false;
         ++n;
       }
       if (pending) issue_pv(t - 1, pend_first, pend_n);
@@ -441,10 +483,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
     bool ok = true;
     int t = 0;
     for (int n = 0; ok; ++n) {
-      const int id = __shfl_sync(kFullMask, next_item(n), 0);
-      if (id < 0) break;
       Item it;
-      load_item(p, id, it);
+      if (take_item_warp(n, it) < 0) break;
       const int pos = it.q0 + r / G;
       const bool row_valid = pos < it.q_len;
       const int limit = it.P + pos;  // last key this row may see
@@ -462,30 +502,32 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         const int kbase = j * kKeys;
         // Tiles below every row's causal limit and inside k_len need no mask (CTA-uniform
         // test); there, with a positive scale, max and exp take the raw scores:
-        // p = 2^(s*c - m). Max and sum use eight partial accumulators to keep dependency chains
-        // short.
+        // p = 2^(s*c - m). Arithmetic runs on pairs (fp32x2 FMA and add) and the max takes
+        // three inputs per instruction, in four chains.
         const bool full = kbase + kKeys - 1 <= it.P + it.q0 && kbase + kKeys <= it.k_len &&
                           p.qk_scale_log2 > 0.f;
-        float part[8];
-        if (full) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(sr[u]);
-#pragma unroll
-          for (int c = 8; c < 64; ++c) part[c & 7] = fmaxf(part[c & 7], __uint_as_float(sr[c]));
-        } else {
+        if (!full) {
           // keys kbase + c with c < nv are unmasked for this row (c <= limit - kbase, inside k_len)
           const int nv = max(0, min(kKeys, min(limit + 1, it.k_len) - kbase));
 #pragma unroll
-          for (int u = 0; u < 8; ++u) part[u] = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float s = c < nv ? __uint_as_float(sr[c]) * p.qk_scale_log2 : -INFINITY;
-            sr[c] = __float_as_uint(s);
-            part[c & 7] = fmaxf(part[c & 7], s);
-          }
+          for (int c = 0; c < 64; ++c)
+            sr[c] = __float_as_uint(c < nv ? __uint_as_float(sr[c]) * p.qk_scale_log2
+                                           : -INFINITY);
         }
-        float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                         fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+        float mt;
+        {
+          auto sv = [&sr](int c) { return __uint_as_float(sr[c]); };
+          float mx[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx[u] = fmax3(sv(u), sv(u + 4), sv(u + 8));
+#pragma unroll
+          for (int k = 3; k < 15; k += 2)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], sv(u + 4 * k), sv(u + 4 * k + 4));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], sv(u + 60));
+          mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+        }
         if (full) mt *= p.qk_scale_log2;
         const bool resc = mt > m_run + kTauP;
         float alpha = 1.f;
@@ -494,31 +536,26 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           m_run = mt;
         }
         uint32_t pk[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) part[u] = 0.f;
-        if (full) {
-          const float c2 = p.qk_scale_log2, nm = -m_run;
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), c2, nm));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), c2, nm));
-            part[(c >> 1) & 7] += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
-        } else {
-          // masked scores are -inf and 2^-inf = 0; a row with no unmasked key yet (m_run = -inf)
-          // has only masked scores here, so any finite offset gives its zeros
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // pair sums of p
+        {
+          // full tiles: x = s*c - m; masked tiles: x = s - m, where masked scores are -inf and
+          // 2^-inf = 0 (a row with no unmasked key yet has m_run = -inf and only masked scores
+          // here, so any finite offset gives its zeros)
           const float mm = m_run == -INFINITY ? 0.f : m_run;
+          const uint64_t mul = full ? pack2(p.qk_scale_log2, p.qk_scale_log2) : pack2(1.f, 1.f);
+          const uint64_t off = pack2(-mm, -mm);
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float p0 = fast_exp2(__uint_as_float(sr[c]) - mm);
-            const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - mm);
-            part[(c >> 1) & 7] += p0 + p1;
+            const float2 x = unpack2(ffma2(
+                pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul, off));
+            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            sum2[(c >> 1) & 3] = fadd2(sum2[(c >> 1) & 3], pack2(p0, p1));
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
         }
-        const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
-                          ((part[4] + part[5]) + (part[6] + part[7]));
+        const float2 s01 = unpack2(fadd2(sum2[0], sum2[1]));
+        const float2 s23 = unpack2(fadd2(sum2[2], sum2[3]));
+        const float sum = (s01.x + s01.y) + (s23.x + s23.y);
         l_run = l_run * alpha + sum;
 
         if (t > 0) {  // the previous P V is done: P buffer free, O stable
@@ -539,8 +576,14 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           for (int cc = 0; cc < kHD / 32; ++cc) {
             uint32_t o[32];
             tmem_ld32(trow + kColO + cc * 32, o);
+            const uint64_t a2 = pack2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            for (int c = 0; c < 32; c += 2) {
+              const float2 v = unpack2(
+                  fmul2(pack2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])), a2));
+              o[c] = __float_as_uint(v.x);
+              o[c + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(trow + kColO + cc * 32, o);
           }
         }
@@ -575,10 +618,13 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[64];
         tmem_ld64(trow + kColO + cc * 64, o);
+        const uint64_t inv2 = pack2(inv, inv);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          w[cc * 32 + c] =
-              pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+        for (int c = 0; c < 32; ++c) {
+          const float2 v = unpack2(
+              fmul2(pack2(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])), inv2));
+          w[cc * 32 + c] = pack_bf16x2(v.x, v.y);
+        }
       }
       // O is in registers: the next item's P V may overwrite it
       tc_fence_before_sync();
