@@ -215,11 +215,14 @@ PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cach
  * Equivalent to pkv_kv_store(k_new, v_new, slot_mapping, num_seqs, ...) followed by
  * pkv_paged_decode(...) when, as in a decode step, slot_mapping[b] is the slot of position
  * context_lens[b] - 1 of sequence b (or -1 for a padded entry with context 0):
- *   - k_new[b], v_new[b] are written to slot_mapping[b] (skipped when -1) by the kernel, before
- *     the copies that read position ctx-1 are issued; attention then reads all ctx positions from
- *     the cache, so the result equals store-then-decode bit for bit;
- *   - a slot that is not the block table's slot of position ctx-1 is still written and raises
- *     PKV_DEVERR_BAD_SLOT; the output row of that sequence is then unspecified.
+ *   - k_new[b], v_new[b] are written to slot_mapping[b] (skipped when -1) by the call's first
+ *     grid, which also plans the attention work; the attention grid starts once that grid is
+ *     complete and reads all ctx positions from the cache, so the result equals
+ *     store-then-decode bit for bit, with one launch fewer;
+ *   - a slot outside the cache is skipped and raises PKV_DEVERR_BAD_SLOT; a slot that is not
+ *     the block table's slot of position ctx-1 (or any slot other than -1 for a sequence of
+ *     context 0) is still written and raises PKV_DEVERR_BAD_SLOT; the output row of that
+ *     sequence is then unspecified.
  *   k_new, v_new  device, [num_seqs, num_kv_heads, head_dim] bf16 (one new token per sequence)
  *   slot_mapping  device, [num_seqs] int32
  * Other arguments as pkv_paged_decode; k_cache and v_cache are written.

@@ -31,6 +31,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may
+// start while the previous kernel in the stream is still running; it must call
+// grid_dependency_wait() before touching any memory that earlier work produces or consumes (the
+// wait returns once the previous grid has completed and its writes are visible). A kernel calls
+// allow_dependent_launch() to let the next such kernel start early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_flag(int* flags, int bit) {
   if (flags != nullptr) atomicOr(flags, bit);
 }

@@ -13,8 +13,8 @@ namespace pkv {
 // of the largest tile (128 tokens).
 constexpr int kSplitQuantum = 128;
 
-// Decode kernel instances: head_dim {128, 64} x query heads per CTA {4, 2, 1} x {plain, fused}.
-constexpr int kDecodeInstances = 12;
+// Decode kernel instances: head_dim {128, 64} x query heads per CTA {4, 2, 1}.
+constexpr int kDecodeInstances = 6;
 
 // State of the library in one CUDA context. Module globals (the device error word, the static
 // decode workspace) and kernel attributes exist once per context, so they are looked up or set
@@ -78,7 +78,8 @@ struct DecodeArgs {
   uint16_t* out;
   DecodeWorkspace ws;
   int* flags;
-  // fused store (all null for a plain decode): newest token of sequence b, [B, Hkv, D]
+  // the step's store (all null for a plain decode): newest token of sequence b, [B, Hkv, D],
+  // written to slot_mapping[b] by the plan grid before the decode grid reads the cache
   const uint16_t* k_new = nullptr;
   const uint16_t* v_new = nullptr;
   const int32_t* slot_mapping = nullptr;

@@ -65,14 +65,6 @@ struct DecodeParams {
   int32_t max_splits;
   int32_t cap_tokens;  // contexts are clamped to this many tokens (table and plan capacity)
   float qk_scale_log2;
-  // Fused store (NEXT step of a decode): the newest token of sequence b comes from k_new[b] /
-  // v_new[b] ([B, Hkv, D]) instead of the cache, and is written to slot_mapping[b].
-  int32_t num_kv_heads;
-  const uint16_t* k_new;
-  const uint16_t* v_new;
-  const int32_t* slot_mapping;
-  uint16_t* k_cache;
-  uint16_t* v_cache;
 };
 
 template <int D, int GH>
@@ -145,7 +137,56 @@ struct PlanParams {
   int32_t head_groups;
   int32_t slots;         // resident CTAs of the decode grid
   int32_t counters_per_seq;  // merge counters per sequence (0 when nothing can be split)
+  // The store of a decode step (pkv_paged_decode_store; k_new == nullptr otherwise): the CTAs
+  // after the first write row b of k_new / v_new ([B, Hkv, D]) to slot slot_mapping[b].
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t row_chunks;  // 16-byte chunks in one token row of all kv heads (Hkv * D / 8)
 };
+
+// The store of a decode step, in the CTAs of the plan grid after the first: row b of k_new / v_new
+// goes to cache slot slot_mapping[b] (-1 is skipped; any other slot outside the cache is skipped
+// and flagged), copied in 16-byte chunks across the grid. A slot that is not the block table's
+// slot of position context_lens[b] - 1 is still written and flagged. The decode grid waits for
+// this whole grid, so its copies read the new rows.
+__device__ void store_new_rows(const PlanParams& pp) {
+  const int rc = pp.row_chunks;
+  const int64_t total = (int64_t)pp.num_seqs * rc;
+  const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+  const int64_t cap = (int64_t)pp.num_blocks * pp.block_size;
+  const int lbs = __ffs(pp.block_size) - 1;
+  for (int64_t i = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int b = (int)(i / rc);
+    const int c = (int)(i - (int64_t)b * rc);
+    const int slot = __ldg(pp.slot_mapping + b);
+    if (slot == -1) continue;
+    const bool writes = slot >= 0 && slot < cap;
+    if (c == 0) {
+      int ctx = __ldg(pp.context_lens + b);
+      ctx = ctx < pp.cap_tokens ? ctx : pp.cap_tokens;
+      bool on_table = false;
+      if (writes && ctx > 0) {
+        const int pos = ctx - 1;
+        const int e = pos >> lbs;
+        const int blk = e < pp.max_blocks ? __ldg(pp.block_tables + (int64_t)b * pp.max_blocks + e)
+                                          : -1;
+        on_table = slot == blk * pp.block_size + (pos & (pp.block_size - 1));
+      }
+      if (!on_table) raise_flag(pp.flags, PKV_DEVERR_BAD_SLOT);
+    }
+    if (!writes) continue;
+    const int64_t src = (int64_t)b * rc + c, dst = (int64_t)slot * rc + c;
+    reinterpret_cast<uint4*>(pp.k_cache)[dst] = __ldg(reinterpret_cast<const uint4*>(pp.k_new) + src);
+    reinterpret_cast<uint4*>(pp.v_cache)[dst] = __ldg(reinterpret_cast<const uint4*>(pp.v_new) + src);
+  }
+}
 
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
                                                          uint32_t* total) {
@@ -175,6 +216,12 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 }
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanParams pp) {
+  // the decode grid may be scheduled now: it sets up its barriers, then waits for this grid
+  allow_dependent_launch();
+  if (blockIdx.x > 0) {
+    store_new_rows(pp);
+    return;
+  }
   __shared__ uint32_t warp_sums[32];
   __shared__ int32_t split_sh;
   const int tid = threadIdx.x;
@@ -360,12 +407,11 @@ __device__ __noinline__ void merge_chunks(const DecodeParams& p, int b, int x, i
 // The decode kernel
 // ---------------------------------------------------------------------------------------------
 
-// kFuse: the decode of pkv_paged_decode_store. The producer warp writes the step's new token to
-// the cache before the copies that read it, so the consumers are the same as the plain decode's.
-template <int D, int GH, bool kFuse>
+template <int D, int GH>
 __global__ void __maxnreg__(168)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ DecodeParams p) {
   using T = Traits<D, GH>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem + T::kOffTiles;
@@ -391,6 +437,9 @@ __global__ void __maxnreg__(168)
     fence_barrier_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent of the plan kernel: everything above overlaps the plan;
+  // nothing below reads memory before the plan (and all earlier work) has completed.
+  grid_dependency_wait();
 
   if (warp == T::kWarps) {
     // =============================== producer warp ===============================
@@ -417,12 +466,15 @@ __global__ void __maxnreg__(168)
       if (lane == 0) c = atomicAdd(p.header, 1u);
       return __shfl_sync(kFullMask, c, 0);
     };
-    // Wait until consumers have released the stage slot about to be reused.
+    // Each stage slot has its own issuing lane (lane == stage): one thread's bulk copies complete
+    // one barrier phase at a time, so copies of several stages issued from one thread would
+    // queue behind each other (at block size 16 a stage is eight 4 KB boxes plus q). The slot's
+    // lane waits until the consumers have released it, then fills it.
     auto acquire = [&](int stage) -> bool {
       int good = 1;
-      if (lane == 0)
+      if (lane == stage)
         good = mbar_wait(empty0 + 8 * stage, ((issue / T::kStages) & 1) ^ 1) ? 1 : 0;
-      return __shfl_sync(kFullMask, good, 0) != 0;
+      return __shfl_sync(kFullMask, good, stage) != 0;
     };
 
     uint32_t c = claim();
@@ -430,7 +482,7 @@ __global__ void __maxnreg__(168)
       const int stage = issue % T::kStages;
       if (c >= total) {
         ok = acquire(stage);
-        if (ok && lane == 0) {
+        if (ok && lane == stage) {
           meta[stage].flags = kMetaDone;
           mbar_arrive(full0 + 8 * stage);
         }
@@ -445,7 +497,7 @@ __global__ void __maxnreg__(168)
       ctx = ctx < p.cap_tokens ? ctx : p.cap_tokens;
       if (ctx <= 0) {
         ok = acquire(stage);
-        if (ok && lane == 0) {
+        if (ok && lane == stage) {
           StageMeta m;
           m.b = b; m.x = x; m.split = 0; m.nsplit = 1;
           m.tok0 = 0; m.tok_end = 0; m.flags = kMetaZero; m.pad = 0;
@@ -463,36 +515,6 @@ __global__ void __maxnreg__(168)
       const int32_t* bt_row = p.block_tables + (int64_t)b * p.max_blocks;
       const uint16_t* qsrc = p.q + ((int64_t)b * p.num_q_heads + x * GH) * D;
       const int kv_head = x / p.groups_per_kv;
-
-      if constexpr (kFuse) {
-        // The fused store: this item holds position ctx - 1, so write the step's new token (this
-        // kv head's K and V rows) to its slot before issuing the copies that read it. Every head
-        // group of the kv head writes the same bytes.
-        if (s == nsplit - 1) {
-          constexpr int kRowChunks = D / 8;  // 16-byte chunks of one row
-          const int slot = __ldg(p.slot_mapping + b);
-          const bool writes = slot >= 0 && slot < p.num_blocks * bs;
-          if (writes && lane < 2 * kRowChunks) {
-            const bool is_k = lane < kRowChunks;
-            const int c16 = lane % kRowChunks;
-            const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                (is_k ? p.k_new : p.v_new) + ((int64_t)b * p.num_kv_heads + kv_head) * D + c16 * 8));
-            *reinterpret_cast<uint4*>((is_k ? p.k_cache : p.v_cache) +
-                                      ((int64_t)slot * p.num_kv_heads + kv_head) * D + c16 * 8) =
-                val;
-            fence_proxy_async_global();
-          }
-          if (lane == 0 && slot != -1) {
-            const int pos = ctx - 1;
-            const int e = pos >> lbs;
-            const int blk = e < p.max_blocks ? __ldg(bt_row + e) : -1;
-            if (!writes || slot != blk * bs + (pos & (bs - 1)))
-              raise_flag(p.flags, PKV_DEVERR_BAD_SLOT);
-          }
-          __syncwarp();
-          fence_proxy_async_global();  // lane 0 issues the copies that read the row
-        }
-      }
 
       for (int tok0 = tok_begin; tok0 < tok_end && ok; tok0 += T::kTileT) {
         const int st = issue % T::kStages;
@@ -531,7 +553,7 @@ __global__ void __maxnreg__(168)
         const bool first = tok0 == tok_begin;
         if (first) bytes += T::kQBytes;
         ok = acquire(st);
-        if (ok && lane == 0) {
+        if (ok && lane == st) {
           StageMeta m;
           m.b = b; m.x = x; m.split = s; m.nsplit = nsplit;
           m.tok0 = tok0; m.tok_end = tok_end;
@@ -881,19 +903,19 @@ __global__ void __maxnreg__(168)
   }
 }
 
-template <int D, int GH, bool kFuse>
+template <int D, int GH>
 cudaError_t configure_instance(int* ctas_per_sm) {
   using T = Traits<D, GH>;
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, GH, kFuse>,
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, GH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
   if (e != cudaSuccess) return e;
   // the largest shared-memory carve-out, so that two CTAs fit on an SM
-  e = cudaFuncSetAttribute(paged_decode_kernel<D, GH, kFuse>,
+  e = cudaFuncSetAttribute(paged_decode_kernel<D, GH>,
                            cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, GH, kFuse>,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, GH>,
                                                     T::kThreads, T::kSmemBytes);
   if (e != cudaSuccess) return e;
   *ctas_per_sm = n < 1 ? 1 : n;
@@ -901,16 +923,13 @@ cudaError_t configure_instance(int* ctas_per_sm) {
 }
 
 // Index of an instance in ContextState::decode_ctas.
-constexpr int decode_instance(int D, int GH, bool fuse) {
-  return (D == 128 ? 0 : 6) + (GH == 4 ? 0 : GH == 2 ? 2 : 4) + (fuse ? 1 : 0);
-}
+constexpr int decode_instance(int D, int GH) { return (D == 128 ? 0 : 3) + (GH == 4 ? 0 : GH == 2 ? 1 : 2); }
 
 template <int D, int GH>
 cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int num_sms, cudaStream_t stream) {
   using T = Traits<D, GH>;
-  const bool fuse = a.k_new != nullptr;
-  const int ctas_per_sm = a.ctas_per_sm[decode_instance(D, GH, fuse)];
+  const int ctas_per_sm = a.ctas_per_sm[decode_instance(D, GH)];
   if (ctas_per_sm <= 0) return cudaErrorInvalidConfiguration;
   const int G = a.num_q_heads / a.cache.num_kv_heads;
   DecodeParams p;
@@ -938,12 +957,6 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   if (cap > 0x7fffffff) cap = 0x7fffffff;
   p.cap_tokens = (int32_t)cap;
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
-  p.num_kv_heads = a.cache.num_kv_heads;
-  p.k_new = a.k_new;
-  p.v_new = a.v_new;
-  p.slot_mapping = a.slot_mapping;
-  p.k_cache = const_cast<uint16_t*>(a.k_cache);
-  p.v_cache = const_cast<uint16_t*>(a.v_cache);
 
   const int64_t upper = (int64_t)a.num_seqs * a.max_splits * p.head_groups;
   int64_t grid = (int64_t)num_sms * ctas_per_sm;
@@ -963,15 +976,41 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   pp.head_groups = p.head_groups;
   pp.slots = (int32_t)((int64_t)num_sms * ctas_per_sm);
   pp.counters_per_seq = a.max_splits > 1 ? p.head_groups * T::kWarps : 0;
-  decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
+  pp.k_new = a.k_new;
+  pp.v_new = a.v_new;
+  pp.slot_mapping = a.slot_mapping;
+  pp.k_cache = const_cast<uint16_t*>(a.k_cache);
+  pp.v_cache = const_cast<uint16_t*>(a.v_cache);
+  pp.block_tables = a.block_tables;
+  pp.max_blocks = a.max_blocks;
+  pp.block_size = a.cache.block_size;
+  pp.num_blocks = a.cache.num_blocks;
+  pp.row_chunks = a.cache.num_kv_heads * D / 8;
+  // One CTA plans; with a store (pkv_paged_decode_store) more CTAs copy the new rows, about four
+  // 16-byte chunks of K and of V per thread.
+  int store_ctas = 0;
+  if (a.k_new != nullptr) {
+    const int64_t chunks = (int64_t)a.num_seqs * pp.row_chunks;
+    const int64_t want = (chunks + 4 * kPlanThreads - 1) / (4 * kPlanThreads);
+    store_ctas = (int)(want < num_sms ? want : num_sms);
+    if (store_ctas < 1) store_ctas = 1;
+  }
+  decode_plan_kernel<<<1 + store_ctas, kPlanThreads, 0, stream>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (fuse)
-    paged_decode_kernel<D, GH, true><<<(unsigned)grid, T::kThreads, T::kSmemBytes, stream>>>(tk, tv, p);
-  else
-    paged_decode_kernel<D, GH, false><<<(unsigned)grid, T::kThreads, T::kSmemBytes, stream>>>(tk, tv,
-                                                                                            p);
-  return cudaGetLastError();
+  // The decode grid is a programmatic dependent of the plan: it is scheduled while the plan runs
+  // and waits for it in-kernel, which hides the launch gap between the two.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(T::kThreads);
+  cfg.dynamicSmemBytes = T::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, GH>, tk, tv, p);
 }
 
 }  // namespace
@@ -1008,10 +1047,8 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t hea
 
 cudaError_t configure_decode_kernels(int (&ctas)[kDecodeInstances]) {
   cudaError_t e = cudaSuccess;
-#define PKV_CONFIGURE(D, GH)                                                                     \
-  if (e == cudaSuccess)                                                                          \
-    e = configure_instance<D, GH, false>(&ctas[decode_instance(D, GH, false)]);                 \
-  if (e == cudaSuccess) e = configure_instance<D, GH, true>(&ctas[decode_instance(D, GH, true)]);
+#define PKV_CONFIGURE(D, GH) \
+  if (e == cudaSuccess) e = configure_instance<D, GH>(&ctas[decode_instance(D, GH)]);
   PKV_CONFIGURE(128, 4)
   PKV_CONFIGURE(128, 2)
   PKV_CONFIGURE(128, 1)
