@@ -95,14 +95,30 @@ PKV_API int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* sl
  *                      < 0 = never split.
  * Outputs: split_tokens (fixed chunk length, or the smallest chunk length when auto_split is 1),
  * max_splits (the most chunks any sequence can have), workspace_bytes (device workspace the
- * decode call needs for these num_seqs and num_q_heads).
+ * decode call needs for these num_seqs and num_q_heads), and engine, always
+ * PKV_DECODE_ENGINE_CUDA_CORE. The caller may set engine before the decode call:
+ *   PKV_DECODE_ENGINE_CUDA_CORE    the persistent decode kernel: CUDA-core fp32 arithmetic,
+ *                                  chunked (split) contexts, any supported shape;
+ *   PKV_DECODE_ENGINE_TENSOR_CORE  the tcgen05 attention kernel with one query row per sequence
+ *                                  (the G query heads of a kv head are the valid rows of one
+ *                                  128-row MMA tile); head_dim 128 and group size 4 or 8 only
+ *                                  (PKV_ERR_UNSUPPORTED otherwise); contexts are never split.
+ *                                  On a B300 it reads K/V about 4% faster in a short burst, but
+ *                                  the unused rows of its MMAs and softmax draw enough power
+ *                                  that a sustained decode loop runs into the power cap (SM
+ *                                  clock ~1.15 GHz against ~1.9 GHz) and ends up ~10% slower.
  */
+#define PKV_DECODE_ENGINE_CUDA_CORE 1
+#define PKV_DECODE_ENGINE_TENSOR_CORE 2
+
 typedef struct pkv_decode_plan {
   int32_t split_tokens;
   int32_t max_splits;
   int32_t auto_split;
   int32_t max_context_len;
   size_t workspace_bytes;
+  int32_t engine;
+  int32_t reserved;
 } pkv_decode_plan;
 
 PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
@@ -127,7 +143,10 @@ PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cach
  *   workspace     device scratch of at least plan->workspace_bytes, 256-byte aligned, owned by
  *                 the caller. Every call rewrites it, so calls that share one workspace must be
  *                 ordered on one stream.
- * Launches: a one-CTA plan kernel (chunking, work list) and the persistent decode kernel.
+ * Launches (engine PKV_DECODE_ENGINE_CUDA_CORE): a one-CTA plan kernel (chunking, work list) and
+ * the persistent decode kernel, launched as its programmatic dependent. With
+ * PKV_DECODE_ENGINE_TENSOR_CORE: the tcgen05 attention kernel alone, whose work counter sits at
+ * the start of the workspace.
  */
 PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                      pkv_cache_desc cache, const int32_t* block_tables,
@@ -216,9 +235,9 @@ PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cach
  * pkv_paged_decode(...) when, as in a decode step, slot_mapping[b] is the slot of position
  * context_lens[b] - 1 of sequence b (or -1 for a padded entry with context 0):
  *   - k_new[b], v_new[b] are written to slot_mapping[b] (skipped when -1) by the call's first
- *     grid, which also plans the attention work; the attention grid starts once that grid is
- *     complete and reads all ctx positions from the cache, so the result equals
- *     store-then-decode bit for bit, with one launch fewer;
+ *     grid (with the CUDA-core engine the same grid also plans the attention work); the
+ *     attention grid starts once that grid is complete and reads all ctx positions from the
+ *     cache, so the result equals store-then-decode bit for bit, with one launch fewer;
  *   - a slot outside the cache is skipped and raises PKV_DEVERR_BAD_SLOT; a slot that is not
  *     the block table's slot of position ctx-1 (or any slot other than -1 for a sequence of
  *     context 0) is still written and raises PKV_DEVERR_BAD_SLOT; the output row of that
@@ -295,7 +314,7 @@ PKV_API const char* pkv_status_string(int status);
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version: major * 10000 + minor * 100 + patch. 0.2.0 added the prefill workspace. */
-#define PKV_VERSION 200
+#define PKV_VERSION 201
 PKV_API int pkv_version(void);
 
 #ifdef __cplusplus

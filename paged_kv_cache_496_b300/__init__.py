@@ -39,6 +39,9 @@ DEVERR_CTX_CLAMPED = 4
 DEVERR_TIMEOUT = 8
 DEVERR_BAD_LENGTHS = 16
 
+DECODE_ENGINE_CUDA_CORE = 1    # PKV_DECODE_ENGINE_CUDA_CORE
+DECODE_ENGINE_TENSOR_CORE = 2  # PKV_DECODE_ENGINE_TENSOR_CORE
+
 
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
@@ -48,7 +51,8 @@ class CacheDesc(ctypes.Structure):
 class DecodePlan(ctypes.Structure):
     _fields_ = [("split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("auto_split", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("engine", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -57,7 +61,7 @@ class PagedKVError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 200  # PKV_VERSION of include/pagedkv.h that the argtypes below describe
+ABI_VERSION = 201  # PKV_VERSION of include/pagedkv.h that the argtypes below describe
 
 
 def _load():
@@ -153,11 +157,15 @@ def kv_store(k, v, slot_mapping, k_cache, v_cache, stream=None):
 
 
 def decode_plan(num_seqs: int, num_q_heads: int, k_cache: torch.Tensor, max_context_len: int,
-                split_tokens: int = 0) -> DecodePlan:
-    """Host-side decode plan (chunking and workspace size); see pkv_decode_plan_make."""
+                split_tokens: int = 0, engine: Optional[int] = None) -> DecodePlan:
+    """Host-side decode plan (chunking, workspace size and engine); see pkv_decode_plan_make.
+    engine: None keeps the library's choice, else DECODE_ENGINE_CUDA_CORE or
+    DECODE_ENGINE_TENSOR_CORE."""
     plan = DecodePlan()
     _check(lib.pkv_decode_plan_make(num_seqs, num_q_heads, _cache_desc(k_cache),
                                     int(max_context_len), int(split_tokens), ctypes.byref(plan)))
+    if engine is not None:
+        plan.engine = int(engine)
     return plan
 
 
@@ -194,7 +202,7 @@ def workspace_for(plan: DecodePlan, device: torch.device, stream=None) -> torch.
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
                  max_context_len: Optional[int] = None, split_tokens: int = 0,
                  plan: Optional[DecodePlan] = None, workspace: Optional[torch.Tensor] = None,
-                 stream=None):
+                 stream=None, engine: Optional[int] = None):
     """Decode attention over the paged cache. Returns out [num_seqs, num_q_heads, head_dim] bf16.
 
     max_context_len bounds context_lens (host int); if omitted it is read from the device (a
@@ -218,7 +226,7 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
     if plan is None:
         if max_context_len is None:
             max_context_len = int(context_lens.max().item()) if B else 0
-        plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens)
+        plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens, engine)
     if workspace is None:
         workspace = workspace_for(plan, q.device, stream)
     _check(lib.pkv_paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
@@ -232,7 +240,8 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
 def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
                        context_lens, scale: float, out=None, max_context_len: Optional[int] = None,
                        split_tokens: int = 0, plan: Optional[DecodePlan] = None,
-                       workspace: Optional[torch.Tensor] = None, stream=None):
+                       workspace: Optional[torch.Tensor] = None, stream=None,
+                       engine: Optional[int] = None):
     """One decode step with the store fused in: writes k_new[b], v_new[b] to slot_mapping[b] and
     attends over context_lens[b] tokens, the last of which is taken from k_new / v_new."""
     _need(q, "q", torch.bfloat16, 3)
@@ -252,7 +261,7 @@ def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_ta
     if plan is None:
         if max_context_len is None:
             max_context_len = int(context_lens.max().item()) if B else 0
-        plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens)
+        plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens, engine)
     if workspace is None:
         workspace = workspace_for(plan, q.device, stream)
     _check(lib.pkv_paged_decode_store(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),

@@ -122,11 +122,20 @@ struct PrefillArgs {
   uint16_t* out;
   int* flags;
   int32_t* item_counter;  // device, in the caller's workspace
+  // Decode on the tensor cores (cu_seqlens_q / cu_seqlens_k unused) when non-null: sequence b
+  // has the single query row b of q [num_seqs, num_q_heads, 128] and context_lens[b] cached keys
+  // (clamped to cap_tokens); max_seqlen_q is 1 and total_q is num_seqs.
+  const int32_t* context_lens = nullptr;
+  int32_t cap_tokens = 0;
 };
 
 // Query positions per 128-row prefill tile, and rows per K/V TMA box.
 int prefill_positions_per_tile(int group);
 int prefill_kv_box_rows(int block_size, bool paged);
+
+// The store of a decode step alone (the plan grid's store CTAs): row b of a.k_new / a.v_new to
+// slot a.slot_mapping[b], checked against the block table.
+cudaError_t launch_decode_store_rows(const DecodeArgs& a, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tmap_q,
                                  const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,

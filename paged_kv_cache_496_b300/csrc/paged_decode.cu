@@ -149,6 +149,7 @@ struct PlanParams {
   int32_t block_size;
   int32_t num_blocks;
   int32_t row_chunks;  // 16-byte chunks in one token row of all kv heads (Hkv * D / 8)
+  int32_t do_plan;     // 0: the grid only stores (CTA 0 has nothing to do)
 };
 
 // The store of a decode step, in the CTAs of the plan grid after the first: row b of k_new / v_new
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
     store_new_rows(pp);
     return;
   }
+  if (!pp.do_plan) return;
   __shared__ uint32_t warp_sums[32];
   __shared__ int32_t split_sh;
   const int tid = threadIdx.x;
@@ -986,6 +988,7 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   pp.block_size = a.cache.block_size;
   pp.num_blocks = a.cache.num_blocks;
   pp.row_chunks = a.cache.num_kv_heads * D / 8;
+  pp.do_plan = 1;
   // One CTA plans; with a store (pkv_paged_decode_store) more CTAs copy the new rows, about four
   // 16-byte chunks of K and of V per thread.
   int store_ctas = 0;
@@ -1057,6 +1060,32 @@ cudaError_t configure_decode_kernels(int (&ctas)[kDecodeInstances]) {
   PKV_CONFIGURE(64, 1)
 #undef PKV_CONFIGURE
   return e;
+}
+
+cudaError_t launch_decode_store_rows(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+  PlanParams pp = {};
+  pp.context_lens = a.context_lens;
+  pp.flags = a.flags;
+  pp.num_seqs = a.num_seqs;
+  const int64_t cap = (int64_t)a.max_blocks * a.cache.block_size;
+  pp.cap_tokens = (int32_t)(cap > 0x7fffffff ? 0x7fffffff : cap);
+  pp.k_new = a.k_new;
+  pp.v_new = a.v_new;
+  pp.slot_mapping = a.slot_mapping;
+  pp.k_cache = const_cast<uint16_t*>(a.k_cache);
+  pp.v_cache = const_cast<uint16_t*>(a.v_cache);
+  pp.block_tables = a.block_tables;
+  pp.max_blocks = a.max_blocks;
+  pp.block_size = a.cache.block_size;
+  pp.num_blocks = a.cache.num_blocks;
+  pp.row_chunks = a.cache.num_kv_heads * a.cache.head_dim / 8;
+  pp.do_plan = 0;
+  const int64_t chunks = (int64_t)a.num_seqs * pp.row_chunks;
+  int64_t ctas = (chunks + 4 * kPlanThreads - 1) / (4 * kPlanThreads);
+  if (ctas > num_sms) ctas = num_sms;
+  if (ctas < 1) ctas = 1;
+  decode_plan_kernel<<<(unsigned)(1 + ctas), kPlanThreads, 0, stream>>>(pp);
+  return cudaGetLastError();
 }
 
 int decode_box_rows(int head_dim, int group, int block_size) {

@@ -94,6 +94,10 @@ struct PrefillParams {
   int32_t box_rows;      // rows per K/V TMA box
   int32_t oob_row;       // a row coordinate past the end of the K/V tensors (zero fill)
   float qk_scale_log2;
+  // Decode (one query row per sequence; cu_q and cu_k unused) when non-null: sequence b has
+  // q row b and context_lens[b] keys, clamped to cap_tokens; context 0 gives zeros.
+  const int32_t* context_lens;
+  int32_t cap_tokens;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -107,27 +111,52 @@ struct Item {
 };
 static_assert(sizeof(Item) / 4 + 1 <= kItemInts, "item slot size");
 
+constexpr int kItemSkip = 0;  // no work (a tile past the sequence's end, or invalid lengths)
+constexpr int kItemWork = 1;
+constexpr int kItemZero = 2;  // decode of a sequence with context 0: its output rows are zeros
+
 // Items are numbered so that the query tiles of one (sequence, kv head) are adjacent, longest
-// first: CTAs that run at the same time then share that head's K/V through L2. Returns false for
-// an item without work (a tile past the sequence's end, or invalid lengths, flagged once).
-__device__ __forceinline__ bool load_item(const PrefillParams& p, int id, Item& it) {
+// first: CTAs that run at the same time then share that head's K/V through L2. Invalid lengths
+// are flagged once per sequence.
+__device__ __forceinline__ int load_item(const PrefillParams& p, int id, Item& it) {
   const int qt = p.num_q_tiles - 1 - id % p.num_q_tiles;
   const int t = id / p.num_q_tiles;
   it.g = t % p.num_kv_heads;
   it.b = t / p.num_kv_heads;
-  it.q_start = __ldg(p.cu_q + it.b);
-  it.q_len = __ldg(p.cu_q + it.b + 1) - it.q_start;
-  it.k_len = __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
+  if (p.context_lens != nullptr) {
+    // decode: query row b attends to all of its context_lens[b] cached keys
+    int ctx = __ldg(p.context_lens + it.b);
+    if (ctx > p.cap_tokens) {
+      if (it.g == 0) raise_flag(p.flags, PKV_DEVERR_CTX_CLAMPED);
+      ctx = p.cap_tokens;
+    }
+    if (ctx <= 0) return kItemZero;
+    it.q_start = it.b;
+    it.q_len = 1;
+    it.k_len = ctx;
+  } else {
+    it.q_start = __ldg(p.cu_q + it.b);
+    it.q_len = __ldg(p.cu_q + it.b + 1) - it.q_start;
+    it.k_len = __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
+  }
   if (it.q_len < 0 || it.k_len < it.q_len) {
     if (threadIdx.x == 0 && qt == 0 && it.g == 0) raise_flag(p.flags, PKV_DEVERR_BAD_LENGTHS);
-    return false;
+    return kItemSkip;
   }
   it.q0 = qt * p.pos_per_tile;
-  if (it.q0 >= it.q_len) return false;
+  if (it.q0 >= it.q_len) return kItemSkip;
   it.P = it.k_len - it.q_len;  // cached prefix length
   const int last_pos = min(it.q_len, it.q0 + p.pos_per_tile) - 1;
   it.n_kt = (it.P + last_pos + 1 + kKeys - 1) / kKeys;
-  return true;
+  return kItemWork;
+}
+
+// Decode of a sequence with context 0 (a padded batch entry): zeros for the G query heads of kv
+// head it.g, written by the producer thread that claimed the item.
+__device__ __forceinline__ void write_zero_rows(const PrefillParams& p, const Item& it) {
+  uint4* dst = reinterpret_cast<uint4*>(
+      p.out + ((int64_t)it.b * p.num_q_heads + it.g * p.group) * kHD);
+  for (int i = 0; i < p.group * kHD / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Persistent: the producer claims item ids in increasing order from a global counter (skipping
@@ -282,10 +311,12 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         while (claimed < p.num_items) {
           const int c = claimed;
           claimed = atomicAdd(p.item_counter, 1);
-          if (load_item(p, c, it)) {
+          const int kind = load_item(p, c, it);
+          if (kind == kItemWork) {
             id = c;
             break;
           }
+          if (kind == kItemZero) write_zero_rows(p, it);
         }
         ok = mbar_wait(bar(kBarItemEmpty + (n & 1)), ((n >> 1) & 1) ^ 1);
         if (ok) {
@@ -687,6 +718,8 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
   p.box_rows = prefill_kv_box_rows(a.cache.block_size, paged);
   p.oob_row = paged ? a.cache.num_blocks * a.cache.block_size : a.total_q;
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
+  p.context_lens = a.context_lens;
+  p.cap_tokens = a.cap_tokens;
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads * a.num_seqs;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidConfiguration;

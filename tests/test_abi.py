@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(pk):
 
 
 def test_status_strings_and_version(pk):
-    assert pk.lib.pkv_version() == pk.ABI_VERSION == 200
+    assert pk.lib.pkv_version() == pk.ABI_VERSION == 201
     assert pk.lib.pkv_status_string(0) == b"ok"
     assert pk.lib.pkv_status_string(-3) == b"workspace too small"
     assert pk.lib.pkv_status_string(12345) == b"unknown status"
@@ -56,6 +56,16 @@ def test_decode_plan_no_split_for_short_contexts(pk):
                                        ctypes.byref(plan)) == 0
     assert plan.max_splits == 1 and plan.auto_split == 0 and plan.split_tokens == 512
     assert plan.workspace_bytes >= 256 + 1024 * 8
+
+
+def test_decode_plan_engine_defaults_to_cuda_core(pk):
+    """pkv_decode_plan_make always picks the CUDA-core engine; the tensor-core one is opt-in."""
+    plan = pk.DecodePlan()
+    for B, hq, ctx, hint in ((1024, 32, 2048, 0), (1024, 64, 2048, -1), (64, 32, 32768, 0)):
+        assert pk.lib.pkv_decode_plan_make(B, hq, _desc(pk, 5000, 256), ctx, hint,
+                                           ctypes.byref(plan)) == 0
+        assert plan.engine == pk.DECODE_ENGINE_CUDA_CORE
+    assert pk.decode_plan.__defaults__[-1] is None
 
 
 def test_decode_plan_auto_and_fixed(pk):
@@ -118,6 +128,11 @@ def test_decode_validation_without_launch(pk):
     assert call(wsb=plan.workspace_bytes - 1) == -3
     assert b"workspace" in pk.lib.pkv_last_error()
     assert call(Hq=12) == -1
+    plan.engine = 7                               # no such engine
+    assert call() == -1
+    plan.engine = pk.DECODE_ENGINE_TENSOR_CORE    # group size 2: no tensor-core instance
+    assert call(Hq=16) == -2
+    assert b"tensor-core" in pk.lib.pkv_last_error()
 
 
 def test_prefill_validation_without_launch(pk):

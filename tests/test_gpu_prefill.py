@@ -245,3 +245,64 @@ def test_mixed_decode_and_prefill_batch(orc):
     out = _prefill_call(q, k, v, cu_q, cu_k, bt, 1 / np.sqrt(D), kcd, vcd)
     ref = orc.paged_prefill(q, k, v, cu_q, cu_k, bt, kc, vc, 1 / np.sqrt(D))
     assert_attn_close(out, ref, what="mixed batch")
+
+
+def _mixed_case(seed, ql, prefix, BS, Hq, Hkv=8, D=128):
+    rng = W.rng_for(seed, 0)
+    ql = np.asarray(ql, np.int32)
+    prefix = np.asarray(prefix, np.int32)
+    kl = ql + prefix
+    bt, nb = W.place_blocks(rng, kl, BS)
+    kc = W.normal_bf16(rng, (nb, BS, Hkv, D))
+    vc = W.normal_bf16(rng, (nb, BS, Hkv, D))
+    T = int(ql.sum())
+    q, k, v = (W.normal_bf16(rng, (T, Hq, D)), W.normal_bf16(rng, (T, Hkv, D)),
+               W.normal_bf16(rng, (T, Hkv, D)))
+    cu_q = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(kl)]).astype(np.int32)
+    seq = np.concatenate([np.full(n, b) for b, n in enumerate(ql)])
+    pos = np.concatenate([prefix[b] + np.arange(n) for b, n in enumerate(ql)])
+    slots = W.slots_for_positions(bt, seq, pos, BS)
+    return dict(q=q, k=k, v=v, kc=kc, vc=vc, bt=bt, cu_q=cu_q, cu_k=cu_k, slots=slots, ql=ql,
+                kl=kl, scale=1 / np.sqrt(D))
+
+
+@pytest.mark.parametrize("BS,Hq", [(16, 32), (256, 32), (64, 64), (32, 16)],
+                         ids=["BS16_G4", "BS256_G4", "BS64_G8", "BS32_G2"])
+def test_mixed_batch_decode_rows_match_decode(orc, BS, Hq):
+    """A paged varlen call mixing decode rows (q_len == 1, long and short contexts) with prefill
+    chunks matches the oracle, and its decode rows match the decode kernel on the same
+    sequences within the tolerance."""
+    c = _mixed_case(70 + BS + Hq, [1, 1, 200, 1, 64, 1, 129, 1, 1],
+                    [300, 1000, 0, 17, 512, 1, 255, 2047, 63], BS, Hq)
+    kcd, vcd = dev_bf16(c["kc"]), dev_bf16(c["vc"])
+    q, k, v = dev_bf16(c["q"]), dev_bf16(c["k"]), dev_bf16(c["v"])
+    pk.kv_store(k, v, dev_i32(c["slots"]), kcd, vcd)
+    out = pk.paged_prefill(q, k, v, dev_i32(c["cu_q"]), dev_i32(c["cu_k"]), dev_i32(c["bt"]),
+                           c["scale"], k_cache=kcd, v_cache=vcd, max_seqlen_q=int(c["ql"].max()))
+    assert pk.get_device_error() == 0
+    ref = orc.paged_prefill(c["q"], c["k"], c["v"], c["cu_q"], c["cu_k"], c["bt"], c["kc"],
+                            c["vc"], c["scale"])
+    assert_attn_close(out, ref, what=f"mixed BS={BS} Hq={Hq}")
+    dec = np.nonzero(c["ql"] == 1)[0]
+    rows = torch.as_tensor(c["cu_q"][dec], device="cuda")
+    d = pk.paged_decode(q[rows], kcd, vcd, dev_i32(c["bt"][dec]), dev_i32(c["kl"][dec]),
+                        c["scale"], max_context_len=int(c["kl"].max()))
+    assert (out[rows].float() - d.float()).abs().max().item() <= TOL
+
+
+def test_all_decode_rows_batch(orc):
+    """Every sequence of a varlen call a decode row (q_len == 1)."""
+    ql = np.ones(37, np.int32)
+    prefix = W.uniform_int(W.rng_for(71, 1), 1, 900, 37).astype(np.int32)
+    c = _mixed_case(71, ql, prefix, 16, 32)
+    kcd, vcd = dev_bf16(c["kc"]), dev_bf16(c["vc"])
+    k, v = dev_bf16(c["k"]), dev_bf16(c["v"])
+    pk.kv_store(k, v, dev_i32(c["slots"]), kcd, vcd)
+    out = pk.paged_prefill(dev_bf16(c["q"]), k, v, dev_i32(c["cu_q"]), dev_i32(c["cu_k"]),
+                           dev_i32(c["bt"]), c["scale"], k_cache=kcd, v_cache=vcd,
+                           max_seqlen_q=1)
+    assert pk.get_device_error() == 0
+    ref = orc.paged_prefill(c["q"], c["k"], c["v"], c["cu_q"], c["cu_k"], c["bt"], c["kc"],
+                            c["vc"], c["scale"])
+    assert_attn_close(out, ref, what="all decode rows")
