@@ -3,8 +3,9 @@
 
 Default workload: Qwen3-8B-shaped decode -- 1024 sequences, context = input U{100..1024} +
 generated U{100..1024}, 32 query / 8 KV heads, head_dim 128, block_size 256, 36 layer caches with
-random physical block placement. One step = for each of the 36 layers: kv_store of the newest
-token of every sequence, then paged decode attention over the whole context.
+random physical block placement. One step = for each of the 36 layers: the store of the newest
+token of every sequence and paged decode attention over the whole context, as one
+pkv_paged_decode_store call (--unfused: pkv_kv_store, then pkv_paged_decode).
 
 Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle on a bounded sample of
 the same workload instead (the only reference implementation of this path).
@@ -76,6 +77,7 @@ def profiled_traffic(kernel_key, source):
 
 PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_prefill.cu")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_decode.cu")
+STORE_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "kv_store.cu")
 
 
 def prefill_profile_keys():
@@ -280,6 +282,46 @@ def measured_tensor_peak():
     return 1800.0, "fallback"
 
 
+def store_arm(args, torch, pk, device):
+    """--workload kv_store_decode | kv_store_prefill: the KV store alone (a component, not the
+    headline), at the decode step's size (1024 tokens, one per Qwen3-8B sequence) or the
+    prefix-cache prefill's (35,968 new tokens), into a Qwen3-8B-shaped layer pool (8 kv heads,
+    head_dim 128, block_size 256). GB/s counts the bytes read and written."""
+    T = 1024 if args.workload == "kv_store_decode" else 35968
+    nb = 5200
+    kc = W.fill_normal_bf16_(torch.empty((nb, 256, 8, 128), dtype=torch.bfloat16, device=device),
+                             6, 1)
+    vc = W.fill_normal_bf16_(torch.empty_like(kc), 6, 2)
+    slots = torch.from_numpy(W.rng_for(6, 3).permutation(nb * 256)[:T].astype(np.int32)).to(
+        device)
+    k = W.fill_normal_bf16_(torch.empty((T, 8, 128), dtype=torch.bfloat16, device=device), 6, 4)
+    v = W.fill_normal_bf16_(torch.empty_like(k), 6, 5)
+    for _ in range(args.warmup):
+        pk.kv_store(k, v, slots, kc, vc)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        pk.kv_store(k, v, slots, kc, vc)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    moved = 2 * 2 * T * 8 * 128 * 2  # K and V, read and written
+    peak, kind = measured_peaks()
+    gbs = moved / ms / 1e6
+    line = {"metric": "KV store GB/s (read + written)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens": T, "num_kv_heads": 8,
+                       "head_dim": 128, "block_size": 256},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_source": kind,
+                         "traffic": profiled_traffic(args.workload, STORE_SRC)},
+            "device_error_flags": pk.get_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def prefill_arm(args, torch, pk, device):
     """--workload prefix_prefill: TFLOP/s of the prefill kernel (a component, not the headline)."""
     ps = PrefillStep(torch, pk, device)
@@ -406,9 +448,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
-    ap.add_argument("--fused", action="store_true",
-                    help="one pkv_paged_decode_store per layer instead of pkv_kv_store then "
-                         "pkv_paged_decode")
+    ap.add_argument("--unfused", action="store_true",
+                    help="pkv_kv_store then pkv_paged_decode per layer instead of one "
+                         "pkv_paged_decode_store (the step's store fused into the decode call)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload (not a bench number)")
     ap.add_argument("--num-seqs", type=int, default=0,
@@ -436,8 +478,10 @@ def main():
 
     if args.workload == "prefix_prefill":
         return prefill_arm(args, torch, pk, device)
+    if args.workload in ("kv_store_decode", "kv_store_prefill"):
+        return store_arm(args, torch, pk, device)
     step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
-                      num_layers=args.layers, fused=args.fused)
+                      num_layers=args.layers, fused=not args.unfused)
     reduced = bool(args.num_seqs or args.layers)
     w = step.w
 
@@ -560,15 +604,16 @@ def main():
                        "mean_context": float(step.ctx.mean()),
                        "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
                        "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
-                       "step": ("per layer: kv_store (1 token/seq) fused into paged_decode"
-                                if step.fused else
+                       "step": ("per layer: one pkv_paged_decode_store (the plan grid also "
+                                "stores the newest token of every sequence; then the persistent "
+                                "decode kernel)" if step.fused else
                                 "per layer: kv_store (1 token/seq), then paged_decode"),
                        "parallelism": f"replicas x{world}",
                        "reduced_for_profiling": reduced},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "paged_decode (plan + persistent decode kernel%s)"
-                                   % (", store fused" if step.fused else ""),
+                         "kernel": "paged_decode (plan%s + persistent decode kernel)"
+                                   % (" grid with the step's store" if step.fused else ""),
                          "algorithmic_bytes_per_launch": step.kv_bytes_per_layer,
                          "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind},
             "clocks": clocks.summary(),
@@ -614,14 +659,16 @@ def secondary_measurements(torch, pk, device, main_step):
     ms = timed(lambda: pk.kv_store(main_step.k_new[0], main_step.v_new[0], main_step.slots_dev,
                                    kc, vc))
     row = main_step.w.kv_bytes_per_token // 2
-    res["kv_store_1024_tokens"] = {"ms": ms, "GB/s": 2 * 2 * main_step.B * row / ms / 1e6}
+    res["kv_store_1024_tokens"] = {"ms": ms, "GB/s": 2 * 2 * main_step.B * row / ms / 1e6,
+                                   "traffic": profiled_traffic("kv_store_decode", STORE_SRC)}
     T = 35968
     rng = W.rng_for(4, 300)
     slots = torch.from_numpy(rng.permutation(main_step.nb * 256)[:T].astype(np.int32)).to(device)
     kn = W.fill_normal_bf16_(torch.empty((T, 8, 128), dtype=torch.bfloat16, device=device),
                              4, 301)
     ms = timed(lambda: pk.kv_store(kn, kn, slots, kc, vc))
-    res["kv_store_35968_tokens"] = {"ms": ms, "GB/s": 2 * 2 * T * row / ms / 1e6}
+    res["kv_store_35968_tokens"] = {"ms": ms, "GB/s": 2 * 2 * T * row / ms / 1e6,
+                                    "traffic": profiled_traffic("kv_store_prefill", STORE_SRC)}
 
     # whole-block moves on the decode pool: 512 copy-on-write copies and a 512-block swap-out
     perm = torch.from_numpy(W.rng_for(3, 500).permutation(main_step.nb)[:1024].astype(np.int32))
@@ -653,7 +700,12 @@ def secondary_measurements(torch, pk, device, main_step):
         ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
                                            layer["ctx"], layer["scale"], out=layer["out"],
                                            plan=layer["plan"], workspace=layer["ws"]))
-        res["long_splitk_decode"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6}
+        lp = profiled("paged_decode_long_splitk", DECODE_SRC) or {}
+        res["long_splitk_decode"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6,
+                                     "frac_of_hbm_peak": layer["kv"] / ms / 1e6 /
+                                     measured_peaks()[0],
+                                     "traffic": lp.get("dram_bytes_per_launch"),
+                                     "dram_throughput_pct": lp.get("dram_throughput_pct_of_peak")}
         del layer
     except Exception as e:  # report, do not hide
         res["long_splitk_decode"] = {"error": repr(e)}
