@@ -275,13 +275,25 @@ PKV_API int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, con
  *       k and v directly; k_cache and v_cache may then be NULL.
  *   out           device, [total_q, num_q_heads, head_dim] bf16
  *   workspace     device, >= PKV_PREFILL_WORKSPACE_BYTES, 16-byte aligned, owned by the caller;
- *                 need not be initialised (the call zeroes its counter on `stream` before the
- *                 kernel). Calls that may run at the same time need distinct workspaces.
- *                 Fewer bytes return PKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *                 need not be initialised (the call resets what must start at zero on `stream`
+ *                 before the attention grid runs). Calls that may run at the same time need
+ *                 distinct workspaces. Fewer bytes return PKV_ERR_WORKSPACE_TOO_SMALL before
+ *                 anything is enqueued. With workspace_bytes >= pkv_prefill_workspace_bytes(
+ *                 num_seqs), a one-CTA plan kernel first numbers only the query tiles each
+ *                 sequence has, so that the attention grid claims no empty work (a decode row
+ *                 in a batch with long prefill rows would otherwise cost ceil(max_seqlen_q /
+ *                 tile) claims); the attention grid is its programmatic dependent.
  * Runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory); supports
  * head_dim 128 and group sizes 1, 2, 4, 8 (other shapes return PKV_ERR_UNSUPPORTED). A persistent
  * grid (two CTAs per SM) claims (sequence, kv head, query tile) items from the counter.
  */
+/*
+ * Workspace bytes with which pkv_paged_prefill numbers a call's work densely (see above):
+ * PKV_PREFILL_WORKSPACE_BYTES plus one int per sequence and one more, rounded up to 256 bytes.
+ * Pure host function; returns PKV_PREFILL_WORKSPACE_BYTES for num_seqs < 0.
+ */
+PKV_API size_t pkv_prefill_workspace_bytes(int32_t num_seqs);
+
 PKV_API int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
                       int32_t total_q, int32_t max_seqlen_q, const int32_t* block_tables,

@@ -80,6 +80,8 @@ def _load():
     L.pkv_paged_decode_store.restype = ctypes.c_int
     L.pkv_paged_decode_store.argtypes = [vp, vp, vp, vp, vp, vp, CacheDesc, vp, i32, vp, i32,
                                          i32, f32, ctypes.POINTER(DecodePlan), vp, vp, sz, vp]
+    L.pkv_prefill_workspace_bytes.restype = ctypes.c_size_t
+    L.pkv_prefill_workspace_bytes.argtypes = [i32]
     L.pkv_paged_prefill.restype = ctypes.c_int
     L.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp, vp,
                                     CacheDesc, i32, f32, vp, vp, sz, vp]
@@ -278,15 +280,23 @@ PREFILL_WORKSPACE_BYTES = 256  # PKV_PREFILL_WORKSPACE_BYTES
 _prefill_ws: dict = {}
 
 
-def prefill_workspace(device: torch.device, stream=None) -> torch.Tensor:
-    """The default prefill workspace (a work counter) of (device, stream), allocated on that
-    stream: calls on one stream share it in order, calls on different streams never race."""
+def prefill_workspace_bytes(num_seqs: int) -> int:
+    """Workspace bytes with which paged_prefill numbers its work densely (no empty query tiles
+    to skip); see pkv_prefill_workspace_bytes."""
+    return int(lib.pkv_prefill_workspace_bytes(int(num_seqs)))
+
+
+def prefill_workspace(device: torch.device, stream=None, num_seqs: int = 0) -> torch.Tensor:
+    """The default prefill workspace of (device, stream), grow-only and allocated on that
+    stream: calls on one stream share it in order, calls on different streams never race. It is
+    sized for num_seqs sequences (dense work numbering)."""
     key, s = _key_and_stream(device, stream)
+    need = prefill_workspace_bytes(num_seqs)
     with _ws_lock:
         ws = _prefill_ws.get(key)
-        if ws is None:
+        if ws is None or ws.numel() < need:
             with torch.cuda.stream(s):
-                ws = torch.empty(PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=key[0])
+                ws = torch.empty(need, dtype=torch.uint8, device=key[0])
             _prefill_ws[key] = ws
         return ws
 
@@ -319,7 +329,7 @@ def paged_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, block_tables, scale: floa
     if max_seqlen_q is None:
         max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
     if workspace is None:
-        workspace = prefill_workspace(q.device, stream)
+        workspace = prefill_workspace(q.device, stream, B)
     _check(lib.pkv_paged_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                  cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Tq,
                                  int(max_seqlen_q), bt_ptr, mb, kc_ptr, vc_ptr, desc, Hq,

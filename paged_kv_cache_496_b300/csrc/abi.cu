@@ -625,10 +625,20 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   a.out = out;
   a.flags = d->flags;
   a.item_counter = static_cast<int32_t*>(workspace);
+  // dense item numbering when the workspace holds the per-sequence prefix after the counter
+  if (workspace_bytes >= pkv_prefill_workspace_bytes(num_seqs))
+    a.item_prefix = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                               PKV_PREFILL_WORKSPACE_BYTES);
   cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d->num_sms,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
   return PKV_OK;
+}
+
+size_t pkv_prefill_workspace_bytes(int32_t num_seqs) {
+  if (num_seqs < 0) return PKV_PREFILL_WORKSPACE_BYTES;
+  const size_t prefix = ((size_t)num_seqs + 1) * sizeof(int32_t);
+  return PKV_PREFILL_WORKSPACE_BYTES + (prefix + 255) / 256 * 256;
 }
 
 }  // extern "C"

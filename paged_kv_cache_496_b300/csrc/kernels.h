@@ -127,6 +127,11 @@ struct PrefillArgs {
   // (clamped to cap_tokens); max_seqlen_q is 1 and total_q is num_seqs.
   const int32_t* context_lens = nullptr;
   int32_t cap_tokens = 0;
+  // Dense item numbering (nullptr: ids run over num_seqs x num_kv_heads x ceil(max_seqlen_q /
+  // positions per tile), and the grid skips the ids of query tiles a sequence does not have):
+  // num_seqs + 1 ints in the caller's workspace, which a one-CTA plan kernel fills with each
+  // sequence's first item id before the attention grid starts.
+  int32_t* item_prefix = nullptr;
 };
 
 // Query positions per 128-row prefill tile, and rows per K/V TMA box.

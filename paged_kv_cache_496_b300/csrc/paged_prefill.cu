@@ -98,6 +98,10 @@ struct PrefillParams {
   // q row b and context_lens[b] keys, clamped to cap_tokens; context 0 gives zeros.
   const int32_t* context_lens;
   int32_t cap_tokens;
+  // Dense numbering when non-null: the items of sequence b are ids item_prefix[b] ..
+  // item_prefix[b + 1] - 1 (its kv heads x its own query tiles), item_prefix[num_seqs] of them
+  // in all; written by prefill_plan_kernel before this grid reads them.
+  const int32_t* item_prefix;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -119,6 +123,27 @@ constexpr int kItemZero = 2;  // decode of a sequence with context 0: its output
 // first: CTAs that run at the same time then share that head's K/V through L2. Invalid lengths
 // are flagged once per sequence.
 __device__ __forceinline__ int load_item(const PrefillParams& p, int id, Item& it) {
+  if (p.item_prefix != nullptr) {
+    // dense numbering: the sequence whose range holds id (binary search over the prefix), then
+    // its kv head and query tile, the longest tile first
+    int lo = 0, hi = p.num_seqs;  // item_prefix[lo] <= id < item_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.item_prefix + mid) <= id) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.q_start = __ldg(p.cu_q + lo);
+    it.q_len = __ldg(p.cu_q + lo + 1) - it.q_start;
+    it.k_len = __ldg(p.cu_k + lo + 1) - __ldg(p.cu_k + lo);
+    const int tiles = (it.q_len + p.pos_per_tile - 1) / p.pos_per_tile;  // >= 1: listed
+    const int local = id - __ldg(p.item_prefix + lo);
+    it.g = local / tiles;
+    it.q0 = (tiles - 1 - local % tiles) * p.pos_per_tile;
+    it.P = it.k_len - it.q_len;
+    const int last_pos = min(it.q_len, it.q0 + p.pos_per_tile) - 1;
+    it.n_kt = (it.P + last_pos + 1 + kKeys - 1) / kKeys;
+    return kItemWork;
+  }
   const int qt = p.num_q_tiles - 1 - id % p.num_q_tiles;
   const int t = id / p.num_q_tiles;
   it.g = t % p.num_kv_heads;
@@ -211,6 +236,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // With dense numbering this grid is a programmatic dependent of the plan kernel: everything
+  // above overlapped the plan; nothing below reads memory before the plan (and all earlier work)
+  // has completed. Without a plan the wait returns at once.
+  grid_dependency_wait();
   // The producer decodes each claimed item once and passes its fields to the other warps through
   // a two-slot ring in shared memory, so that no consumer reloads the sequence lengths from
   // global memory when it moves to the next item.
@@ -302,13 +331,15 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       }
       return true;
     };
+    const int num_items = p.item_prefix != nullptr ? __ldg(p.item_prefix + p.num_seqs)
+                                                   : p.num_items;
     int claimed = lane == 0 ? atomicAdd(p.item_counter, 1) : 0;
     while (ok) {
       // next item with work, or -1; the claim after it is issued now and used later
       int id = -1;
       Item it;
       if (lane == 0) {
-        while (claimed < p.num_items) {
+        while (claimed < num_items) {
           const int c = claimed;
           claimed = atomicAdd(p.item_counter, 1);
           const int kind = load_item(p, c, it);
@@ -681,6 +712,62 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 
 }  // namespace
 
+// Dense item numbering: item_prefix[b] = the items (kv heads x query tiles) of the sequences
+// before b, item_prefix[num_seqs] = all of them; sequences with invalid lengths have none and are
+// flagged here. Also zeroes the grid's work counter. One CTA; the attention grid is its
+// programmatic dependent.
+constexpr int kPlanThreadsP = 1024;
+__global__ void __launch_bounds__(kPlanThreadsP) prefill_plan_kernel(
+    const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs, int32_t pos_per_tile,
+    int32_t num_kv_heads, int32_t* item_prefix, int32_t* item_counter, int* flags) {
+  allow_dependent_launch();
+  __shared__ int64_t warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (num_seqs + kPlanThreadsP - 1) / kPlanThreadsP;
+  const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+  auto items_of = [&](int b) -> int64_t {
+    const int q_len = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
+    const int k_len = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
+    if (q_len < 0 || k_len < q_len) {
+      raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
+      return 0;
+    }
+    return (int64_t)((q_len + pos_per_tile - 1) / pos_per_tile) * num_kv_heads;
+  };
+  int64_t local = 0;
+  for (int b = b0; b < b1; ++b) local += items_of(b);
+  // exclusive scan of the per-thread totals over the CTA
+  int64_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(kFullMask, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  int64_t at = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+  const int64_t total = warp_sums[31];
+  for (int b = b0; b < b1; ++b) {
+    item_prefix[b] = (int32_t)(at < 0x7fffffff ? at : 0x7fffffff);
+    at += items_of(b);
+  }
+  if (tid == 0) {
+    item_prefix[num_seqs] = (int32_t)(total < 0x7fffffff ? total : 0x7fffffff);
+    if (total > 0x7fffffff) raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
+    *item_counter = 0;
+  }
+}
+
 int prefill_positions_per_tile(int group) { return kRows / group; }
 
 cudaError_t configure_prefill_kernel() {
@@ -720,18 +807,41 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
   p.context_lens = a.context_lens;
   p.cap_tokens = a.cap_tokens;
+  p.item_prefix = a.item_prefix;
+  // upper bound of the item count (the exact count, with dense numbering, is on the device)
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads * a.num_seqs;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidConfiguration;
   p.num_items = (int32_t)items;
   p.item_counter = a.item_counter;
-  cudaError_t e = cudaMemsetAsync(a.item_counter, 0, sizeof(int32_t), stream);
-  if (e != cudaSuccess) return e;
   // two CTAs fit on an SM (registers, shared memory, 2 x 256 TMEM columns)
   const int64_t slots = 2 * (int64_t)(num_sms > 0 ? num_sms : 148);
   const unsigned grid = (unsigned)(items < slots ? items : slots);
-  paged_prefill_kernel<<<grid, kThreadsP, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  if (a.item_prefix == nullptr) {
+    cudaError_t e = cudaMemsetAsync(a.item_counter, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    paged_prefill_kernel<<<grid, kThreadsP, kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
+  prefill_plan_kernel<<<1, kPlanThreadsP, 0, stream>>>(a.cu_seqlens_q, a.cu_seqlens_k,
+                                                       a.num_seqs, p.pos_per_tile,
+                                                       p.num_kv_heads, a.item_prefix,
+                                                       a.item_counter, a.flags);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the attention grid is a programmatic dependent of the plan: scheduled while the plan runs,
+  // it waits for it in-kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreadsP);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq, tk, tv, p);
 }
 
 }  // namespace pkv

@@ -153,6 +153,17 @@ def test_prefill_validation_without_launch(pk):
     assert b"workspace_bytes" in pk.lib.pkv_last_error()
 
 
+def test_prefill_workspace_bytes_for_dense_numbering(pk):
+    """The prefill counter (256 B), then one int per sequence and one more, rounded to 256 B."""
+    f = pk.lib.pkv_prefill_workspace_bytes
+    assert f(-1) == 256
+    assert f(0) == 512
+    assert f(63) == 512
+    assert f(64) == 768
+    assert f(1000) == 256 + 4096
+    assert pk.prefill_workspace_bytes(64) == f(64)
+
+
 def test_binding_refuses_cpu_tensors(pk):
     import torch
     k = torch.zeros(4, 8, 128, dtype=torch.bfloat16)

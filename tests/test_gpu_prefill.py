@@ -306,3 +306,45 @@ def test_all_decode_rows_batch(orc):
     ref = orc.paged_prefill(c["q"], c["k"], c["v"], c["cu_q"], c["cu_k"], c["bt"], c["kc"],
                             c["vc"], c["scale"])
     assert_attn_close(out, ref, what="all decode rows")
+
+
+@pytest.mark.parametrize("which", ["mixed", "no_prefix", "prefix"])
+def test_dense_and_sparse_item_numbering_agree(which):
+    """With a workspace of pkv_prefill_workspace_bytes(num_seqs) the work is numbered densely
+    (a plan kernel lists only the query tiles each sequence has); with PREFILL_WORKSPACE_BYTES
+    the grid skips the ids of missing tiles. Every item is computed the same way, so the outputs
+    are bit-identical."""
+    if which == "mixed":
+        c = _mixed_case(72, [1, 1, 300, 1, 64, 0, 129, 1], [300, 1000, 0, 17, 512, 3, 255, 63],
+                        16, 32)
+        bt, kc, vc = dev_i32(c["bt"]), dev_bf16(c["kc"]), dev_bf16(c["vc"])
+        pk.kv_store(dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["slots"]), kc, vc)
+        args = (dev_bf16(c["q"]), dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["cu_q"]),
+                dev_i32(c["cu_k"]), bt, c["scale"])
+        kw = dict(k_cache=kc, v_cache=vc, max_seqlen_q=300)
+        B = len(c["ql"])
+    elif which == "no_prefix":
+        rng = W.rng_for(73, 0)
+        ql = np.array([64, 1, 200, 0, 3, 130], np.int32)
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        T = int(ql.sum())
+        args = (dev_bf16(W.normal_bf16(rng, (T, 32, 128))), dev_bf16(W.normal_bf16(rng, (T, 8, 128))),
+                dev_bf16(W.normal_bf16(rng, (T, 8, 128))), dev_i32(cu), dev_i32(cu), None,
+                1 / np.sqrt(128))
+        kw = dict(max_seqlen_q=200)
+        B = len(ql)
+    else:
+        case = W.prefix_prefill_case(74, 5, 256, 1, 300, 32, 8, 128, 64)
+        kc, vc = dev_bf16(case.k_cache), dev_bf16(case.v_cache)
+        k, v = dev_bf16(case.k), dev_bf16(case.v)
+        pk.kv_store(k, v, dev_i32(case.slot_mapping), kc, vc)
+        args = (dev_bf16(case.q), k, v, dev_i32(case.cu_seqlens_q), dev_i32(case.cu_seqlens_k),
+                dev_i32(case.block_tables), case.scale)
+        kw = dict(k_cache=kc, v_cache=vc, max_seqlen_q=int(case.q_lens.max()))
+        B = case.num_seqs
+    dense_ws = torch.empty(pk.prefill_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    sparse_ws = torch.empty(pk.PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    a = pk.paged_prefill(*args, workspace=dense_ws, **kw)
+    b = pk.paged_prefill(*args, workspace=sparse_ws, **kw)
+    assert pk.get_device_error() == 0
+    assert torch.equal(a, b)
