@@ -77,6 +77,20 @@ def profiled_traffic(kernel_key, source):
 
 PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_prefill.cu")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_decode.cu")
+DECODE_TC_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "paged_decode_tc.cu")
+
+
+def decode_engine_name(pk, engine):
+    return "tensor_core" if engine == pk.DECODE_ENGINE_TENSOR_CORE else "cuda_core"
+
+
+def decode_profile(pk, engine, workload_key):
+    """(profile key, kernel source) of the decode kernel an engine runs, for profiles/traffic.json
+    lookups: the CUDA-core kernel's entries are paged_decode_<workload>, the tensor-core kernel's
+    paged_decode_tc_<workload>."""
+    if engine == pk.DECODE_ENGINE_TENSOR_CORE:
+        return "paged_decode_tc_" + workload_key, DECODE_TC_SRC
+    return "paged_decode_" + workload_key, DECODE_SRC
 STORE_SRC = os.path.join(ROOT, "paged_kv_cache_496_b300", "csrc", "kv_store.cu")
 
 
@@ -169,7 +183,7 @@ class DecodeStep:
     """All layers of one decode step, resident in HBM."""
 
     def __init__(self, name, torch, pk, device, log_fill=True, num_seqs=None, num_layers=None,
-                 fused=False):
+                 fused=False, engine=None):
         self.w = w = W.WORKLOADS[name]
         self.torch, self.pk = torch, pk
         self.ctx = W.decode_lengths(name)
@@ -206,7 +220,8 @@ class DecodeStep:
         self.ctx_dev = torch.from_numpy(self.ctx).to(device)
         self.slots_dev = torch.from_numpy(self.slots).to(device)
         self.scale = 1.0 / np.sqrt(w.head_dim)
-        self.plan = pk.decode_plan(self.B, w.num_q_heads, self.pools[0][0], int(self.ctx.max()), 0)
+        self.plan = pk.decode_plan(self.B, w.num_q_heads, self.pools[0][0], int(self.ctx.max()), 0,
+                                   engine)
         self.ws = torch.empty(max(256, self.plan.workspace_bytes), dtype=torch.uint8,
                               device=device)
         self.kv_bytes_per_layer = int(self.ctx.sum()) * w.kv_bytes_per_token
@@ -455,6 +470,8 @@ def main():
                     help="profiling only: fewer layers than the workload (not a bench number)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling only: the first N sequences (not a bench number)")
+    ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"],
+                    help="decode engine (auto: the library's choice for the shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -480,8 +497,11 @@ def main():
         return prefill_arm(args, torch, pk, device)
     if args.workload in ("kv_store_decode", "kv_store_prefill"):
         return store_arm(args, torch, pk, device)
+    engine = {"auto": None, "cuda_core": pk.DECODE_ENGINE_CUDA_CORE,
+              "tensor_core": pk.DECODE_ENGINE_TENSOR_CORE}[args.engine]
     step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
-                      num_layers=args.layers, fused=not args.unfused)
+                      num_layers=args.layers, fused=not args.unfused, engine=engine)
+    engine_name = decode_engine_name(pk, step.plan.engine)
     reduced = bool(args.num_seqs or args.layers)
     w = step.w
 
@@ -521,7 +541,8 @@ def main():
     tokens_per_s = job_throughput(step.B, ms / 1e3, world)
     peak, peak_kind = measured_peaks()
     achieved = step.kv_bytes_per_layer / (decode_ms_mean / 1e3) / 1e9
-    traffic = profiled_traffic("paged_decode_qwen3_8b", DECODE_SRC)
+    prof_key, prof_src = decode_profile(pk, step.plan.engine, "qwen3_8b")
+    traffic = profiled_traffic(prof_key, prof_src) if args.workload == "qwen3_8b_decode" else None
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -608,12 +629,15 @@ def main():
                                 "stores the newest token of every sequence; then the persistent "
                                 "decode kernel)" if step.fused else
                                 "per layer: kv_store (1 token/seq), then paged_decode"),
+                       "decode_engine": engine_name,
                        "parallelism": f"replicas x{world}",
                        "reduced_for_profiling": reduced},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "paged_decode (plan%s + persistent decode kernel)"
-                                   % (" grid with the step's store" if step.fused else ""),
+                         "kernel": "paged_decode (plan%s + %s)"
+                                   % (" grid with the step's store" if step.fused else "",
+                                      "paged_decode_tc_kernel" if engine_name == "tensor_core"
+                                      else "paged_decode_kernel"),
                          "algorithmic_bytes_per_launch": step.kv_bytes_per_layer,
                          "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind},
             "clocks": clocks.summary(),
@@ -653,6 +677,21 @@ def secondary_measurements(torch, pk, device, main_step):
     main_step.fused = was
     res["fused_step" if not was else "unfused_step"] = {
         "ms": ms, "GB/s": main_step.kv_bytes_per_layer * main_step.L / ms / 1e6}
+
+    # the same step on the other decode engine (the library picks one per shape)
+    plan = main_step.plan
+    other = (pk.DECODE_ENGINE_CUDA_CORE if plan.engine == pk.DECODE_ENGINE_TENSOR_CORE
+             else pk.DECODE_ENGINE_TENSOR_CORE)
+    try:
+        main_step.plan = pk.decode_plan(main_step.B, main_step.w.num_q_heads,
+                                        main_step.pools[0][0], int(main_step.ctx.max()), 0, other)
+        ms = timed(main_step.run, reps=5)
+        res["step_on_" + decode_engine_name(pk, other)] = {
+            "ms": ms, "GB/s": main_step.kv_bytes_per_layer * main_step.L / ms / 1e6}
+    except Exception as e:  # the other engine may not support the shape: report it
+        res["step_on_" + decode_engine_name(pk, other)] = {"error": repr(e)}
+    finally:
+        main_step.plan = plan
 
     # kv_store alone at the decode size (launch-bound) and at the prefill size (bandwidth-bound)
     kc, vc = main_step.pools[0]
@@ -700,8 +739,9 @@ def secondary_measurements(torch, pk, device, main_step):
         ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
                                            layer["ctx"], layer["scale"], out=layer["out"],
                                            plan=layer["plan"], workspace=layer["ws"]))
-        lp = profiled("paged_decode_long_splitk", DECODE_SRC) or {}
+        lp = profiled(*decode_profile(pk, layer["plan"].engine, "long_splitk")) or {}
         res["long_splitk_decode"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6,
+                                     "decode_engine": decode_engine_name(pk, layer["plan"].engine),
                                      "frac_of_hbm_peak": layer["kv"] / ms / 1e6 /
                                      measured_peaks()[0],
                                      "traffic": lp.get("dram_bytes_per_launch"),
@@ -757,6 +797,7 @@ def _qwen3_0p6b_step(torch, pk, device, steps=10):
            "decode_tokens_per_s": st.B / (ms / 1e3), "frac_of_hbm_peak": kv_step / ms / 1e6 / peak,
            "decode_mean_launch_ms": dec_ms, "decode_frac": achieved / peak,
            "num_seqs": st.B, "num_layers": st.L, "distinct_layer_pools": st.n_pools,
+           "decode_engine": decode_engine_name(pk, st.plan.engine),
            "kv_bytes_per_step": kv_step, "flags": pk.get_device_error()}
     del st
     torch.cuda.empty_cache()

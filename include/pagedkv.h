@@ -95,18 +95,22 @@ PKV_API int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* sl
  *                      < 0 = never split.
  * Outputs: split_tokens (fixed chunk length, or the smallest chunk length when auto_split is 1),
  * max_splits (the most chunks any sequence can have), workspace_bytes (device workspace the
- * decode call needs for these num_seqs and num_q_heads), and engine, always
- * PKV_DECODE_ENGINE_CUDA_CORE. The caller may set engine before the decode call:
+ * decode call needs for these num_seqs and num_q_heads), and engine. The plan picks
+ * PKV_DECODE_ENGINE_TENSOR_CORE when head_dim is 128, block_size >= 128 and the group size
+ * G = num_q_heads / num_kv_heads is 4 or 8, and PKV_DECODE_ENGINE_CUDA_CORE otherwise. The caller
+ * may change engine before the decode call:
  *   PKV_DECODE_ENGINE_CUDA_CORE    the persistent decode kernel: CUDA-core fp32 arithmetic,
- *                                  chunked (split) contexts, any supported shape;
- *   PKV_DECODE_ENGINE_TENSOR_CORE  the tcgen05 attention kernel with one query row per sequence
- *                                  (the G query heads of a kv head are the valid rows of one
- *                                  128-row MMA tile); head_dim 128 and group size 4 or 8 only
- *                                  (PKV_ERR_UNSUPPORTED otherwise); contexts are never split.
- *                                  On a B300 it reads K/V about 4% faster in a short burst, but
- *                                  the unused rows of its MMAs and softmax draw enough power
- *                                  that a sustained decode loop runs into the power cap (SM
- *                                  clock ~1.15 GHz against ~1.9 GHz) and ends up ~10% slower.
+ *                                  any supported shape.
+ *   PKV_DECODE_ENGINE_TENSOR_CORE  tcgen05 MMAs with 128 keys of one kv head on the M dimension
+ *                                  and that kv head's G query heads on N (P in bf16, fp32
+ *                                  accumulation); head_dim 128 only (PKV_ERR_UNSUPPORTED
+ *                                  otherwise), any group size, chunked contexts as above.
+ * Both give the same results within bf16 rounding. Measured on a B300 (1024 sequences, 32/8
+ * heads, block_size 256): the tensor-core engine streams K/V at the copy bandwidth and runs a
+ * sustained decode loop at full SM clock; the CUDA-core engine issues about twice the
+ * instructions per byte at G >= 4 and is ~5% slower there. At G <= 2 the CUDA-core engine is
+ * the faster one, and below block_size 128 the TMA boxes of the tensor-core engine (one per
+ * block and 64-dim half) become too small to keep HBM busy.
  */
 #define PKV_DECODE_ENGINE_CUDA_CORE 1
 #define PKV_DECODE_ENGINE_TENSOR_CORE 2
@@ -143,10 +147,8 @@ PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cach
  *   workspace     device scratch of at least plan->workspace_bytes, 256-byte aligned, owned by
  *                 the caller. Every call rewrites it, so calls that share one workspace must be
  *                 ordered on one stream.
- * Launches (engine PKV_DECODE_ENGINE_CUDA_CORE): a one-CTA plan kernel (chunking, work list) and
- * the persistent decode kernel, launched as its programmatic dependent. With
- * PKV_DECODE_ENGINE_TENSOR_CORE: the tcgen05 attention kernel alone, whose work counter sits at
- * the start of the workspace.
+ * Launches: a one-CTA plan kernel (chunking, work list) and the persistent decode kernel of the
+ * plan's engine, launched as its programmatic dependent.
  */
 PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                      pkv_cache_desc cache, const int32_t* block_tables,

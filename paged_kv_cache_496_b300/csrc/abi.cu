@@ -134,6 +134,8 @@ int context_state(const ContextState** out) {
   if (e != cudaSuccess) return cuda_fail(e, "prefill kernel attributes");
   e = configure_decode_kernels(s.decode_ctas);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel attributes");
+  e = configure_decode_tc_kernels();
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core decode kernel attributes");
   g_contexts.push_back(new ContextState(s));
   *out = g_contexts.back();
   return PKV_OK;
@@ -362,75 +364,14 @@ int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c
   pl.workspace_bytes =
       decode_workspace_bytes(num_seqs, num_q_heads, cache.head_dim, pl.max_splits, nullptr,
                              nullptr);
-  // The CUDA-core engine by default: the tensor-core one wastes most of its MMA rows on one query
-  // row per sequence, and under sustained decode that power sends the GPU into its power cap.
-  pl.engine = PKV_DECODE_ENGINE_CUDA_CORE;
-  *plan = pl;
-  return PKV_OK;
-}
-
-// Decode on the tcgen05 attention kernel: one query row per sequence (q [num_seqs, Hq, 128]),
-// keys through the block table, no split; the work counter is the workspace header's first
-// word. With k_new, the step's store runs first, in the plan grid's store CTAs.
-static int decode_tensor_core(const ContextState* d, const uint16_t* q, const uint16_t* k_cache,
-                              const uint16_t* v_cache, const pkv_cache_desc& cache,
-                              const int32_t* block_tables, int32_t max_blocks,
-                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                              float scale, uint16_t* out, uint32_t* counter, void* stream,
-                              const uint16_t* k_new, const uint16_t* v_new,
-                              const int32_t* slot_mapping) {
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The tensor-core engine where it is the faster one on a B300: head_dim 128, blocks of at least
+  // 128 rows (one TMA box per block and 64-dim half stays large) and G >= 4 (the CUDA-core
+  // kernel's arithmetic per byte grows with G and it becomes issue-bound).
   const int G = num_q_heads / cache.num_kv_heads;
-  if (k_new != nullptr) {
-    DecodeArgs sa;
-    sa.k_cache = k_cache;
-    sa.v_cache = v_cache;
-    sa.cache = cache;
-    sa.block_tables = block_tables;
-    sa.max_blocks = max_blocks;
-    sa.context_lens = context_lens;
-    sa.num_seqs = num_seqs;
-    sa.flags = d->flags;
-    sa.k_new = k_new;
-    sa.v_new = v_new;
-    sa.slot_mapping = slot_mapping;
-    const cudaError_t e = launch_decode_store_rows(sa, d->num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decode store launch");
-  }
-  CUtensorMap tq, tk, tv;
-  int st = encode_rows_map(&tq, q, num_seqs, num_q_heads, 128, 64, prefill_positions_per_tile(G),
-                           CU_TENSOR_MAP_SWIZZLE_128B, G);
-  if (st != PKV_OK) return st;
-  const int box = prefill_kv_box_rows(cache.block_size, true);
-  const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
-  st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, 128, 64, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != PKV_OK) return st;
-  st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, 128, 64, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != PKV_OK) return st;
-  PrefillArgs a;
-  a.q = q;
-  a.k = nullptr;
-  a.v = nullptr;
-  a.cu_seqlens_q = nullptr;
-  a.cu_seqlens_k = nullptr;
-  a.num_seqs = num_seqs;
-  a.total_q = num_seqs;
-  a.max_seqlen_q = 1;
-  a.block_tables = block_tables;
-  a.max_blocks = max_blocks;
-  a.cache = cache;
-  a.num_q_heads = num_q_heads;
-  a.scale = scale;
-  a.out = out;
-  a.flags = d->flags;
-  a.item_counter = reinterpret_cast<int32_t*>(counter);
-  a.context_lens = context_lens;
-  const int64_t cap = (int64_t)max_blocks * cache.block_size;
-  a.cap_tokens = (int32_t)(cap > 0x7fffffff ? 0x7fffffff : cap);
-  const cudaError_t e = launch_paged_prefill(a, tq, tk, tv, d->num_sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "tensor-core decode launch");
+  pl.engine = cache.head_dim == 128 && cache.block_size >= 128 && G >= 4
+                  ? PKV_DECODE_ENGINE_TENSOR_CORE
+                  : PKV_DECODE_ENGINE_CUDA_CORE;
+  *plan = pl;
   return PKV_OK;
 }
 
@@ -456,10 +397,9 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
     return fail(PKV_ERR_INVALID_ARG, "decode plan engine %d", plan->engine);
   const int G = num_q_heads / cache.num_kv_heads;
   const bool tc = plan->engine == PKV_DECODE_ENGINE_TENSOR_CORE;
-  if (tc && (cache.head_dim != 128 || (G != 4 && G != 8)))
-    return fail(PKV_ERR_UNSUPPORTED,
-                "tensor-core decode needs head_dim 128 and group size 4 or 8 (got %d, %d)",
-                cache.head_dim, G);
+  if (tc && cache.head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "tensor-core decode needs head_dim 128 (got %d)",
+                cache.head_dim);
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
     return fail(PKV_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
@@ -478,20 +418,6 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
                 workspace_bytes, need);
   const ContextState* d = nullptr;
   st = context_state(&d);
-  if (st != PKV_OK) return st;
-  if (tc)
-    return decode_tensor_core(d, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
-                              context_lens, num_seqs, num_q_heads, scale, out, a.ws.header,
-                              stream, k_new, v_new, slot_mapping);
-  const int box_t = decode_box_rows(cache.head_dim, num_q_heads / cache.num_kv_heads,
-                                    cache.block_size);
-  CUtensorMap tk, tv;
-  const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
-  st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
-                       box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st != PKV_OK) return st;
-  st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
-                       box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != PKV_OK) return st;
   a.q = q;
   a.k_cache = k_cache;
@@ -512,7 +438,40 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
   a.v_new = v_new;
   a.slot_mapping = slot_mapping;
   a.ctas_per_sm = d->decode_ctas;
-  cudaError_t e = launch_paged_decode(a, tk, tv, d->num_sms, static_cast<cudaStream_t>(stream));
+  const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
+  CUtensorMap tk, tv;
+  cudaError_t e = cudaSuccess;
+  if (tc) {
+    // keys on the MMA's M dimension: 128-byte swizzled boxes of 64 dims; q as G rows per box
+    CUtensorMap tq;
+    st = encode_rows_map(&tq, q, num_seqs, num_q_heads, 128, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, G);
+    if (st != PKV_OK) return st;
+    const int box = decode_tc_box_rows(cache.block_size);
+    st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, 128, 64, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != PKV_OK) return st;
+    st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, 128, 64, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != PKV_OK) return st;
+    // boxes of 64 and 32 rows for partial last tiles (only used where smaller than `box`)
+    CUtensorMap tail[4];
+    for (int i = 0; i < 4; ++i) {
+      const int r = (i < 2 ? 64 : 32) < box ? (i < 2 ? 64 : 32) : box;
+      st = encode_rows_map(&tail[i], (i & 1) ? v_cache : k_cache, rows, cache.num_kv_heads, 128,
+                           64, r, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != PKV_OK) return st;
+    }
+    e = launch_paged_decode_tc(a, tq, tk, tv, tail, d->num_sms, static_cast<cudaStream_t>(stream));
+  } else {
+    const int box_t = decode_box_rows(cache.head_dim, G, cache.block_size);
+    st = encode_rows_map(&tk, k_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
+                         box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != PKV_OK) return st;
+    st = encode_rows_map(&tv, v_cache, rows, cache.num_kv_heads, cache.head_dim, cache.head_dim,
+                         box_t, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != PKV_OK) return st;
+    e = launch_paged_decode(a, tk, tv, d->num_sms, static_cast<cudaStream_t>(stream));
+  }
   if (e == cudaErrorNotSupported) return fail(PKV_ERR_UNSUPPORTED, "no decode instance");
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;

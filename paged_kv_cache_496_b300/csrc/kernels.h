@@ -101,6 +101,26 @@ cudaError_t launch_block_hashes(const int32_t* token_ids, const int32_t* cu_seql
 // Rows of the K/V TMA box the decode kernel expects (tile tokens, or the block size if smaller).
 int decode_box_rows(int head_dim, int group, int block_size);
 
+// The plan grid of a decode call: one CTA turns context_lens into the chunk length and the
+// longest-first list of (sequence, chunk) items for a decode grid with `slots` resident CTAs and
+// head_groups items per (sequence, chunk), and resets the claim counter and the first
+// counters_per_seq merge counters of every split sequence; with a.k_new, more CTAs store the
+// step's new rows. The decode grid is launched after it as a programmatic dependent.
+cudaError_t launch_decode_plan(const DecodeArgs& a, int32_t head_groups, int32_t slots,
+                               int32_t counters_per_seq, int32_t cap_tokens, int num_sms,
+                               cudaStream_t stream);
+
+// Decode on the tensor cores with keys on the MMA's M dimension (head_dim 128, any group size):
+// its shared-memory opt-in, the rows of its K/V TMA boxes (128-byte swizzle, 64 dims wide), and
+// the plan plus decode launch. q is read through tmap_q (boxes of 64 dims x G heads x 1 row),
+// K/V through tmap_k/tmap_v (boxes of decode_tc_box_rows rows) and, for a chunk's partial last
+// tile, through tail[] = {K, V with 64-row boxes, K, V with 32-row boxes}.
+cudaError_t configure_decode_tc_kernels();
+int decode_tc_box_rows(int block_size);
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& tmap_q,
+                                   const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                   const CUtensorMap* tail, int num_sms, cudaStream_t stream);
+
 // Returns a CUDA error, or cudaErrorNotSupported for shapes without an instance.
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                 const CUtensorMap& tmap_v, int num_sms, cudaStream_t stream);

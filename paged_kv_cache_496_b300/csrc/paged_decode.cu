@@ -965,41 +965,9 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
 
-  PlanParams pp;
-  pp.context_lens = a.context_lens;
-  pp.items = a.ws.items;
-  pp.header = a.ws.header;
-  pp.counters = a.ws.counters;
-  pp.flags = a.flags;
-  pp.num_seqs = a.num_seqs;
-  pp.cap_tokens = p.cap_tokens;
-  pp.split_floor = a.split_tokens;
-  pp.fixed_split = a.auto_split ? 0 : a.split_tokens;
-  pp.head_groups = p.head_groups;
-  pp.slots = (int32_t)((int64_t)num_sms * ctas_per_sm);
-  pp.counters_per_seq = a.max_splits > 1 ? p.head_groups * T::kWarps : 0;
-  pp.k_new = a.k_new;
-  pp.v_new = a.v_new;
-  pp.slot_mapping = a.slot_mapping;
-  pp.k_cache = const_cast<uint16_t*>(a.k_cache);
-  pp.v_cache = const_cast<uint16_t*>(a.v_cache);
-  pp.block_tables = a.block_tables;
-  pp.max_blocks = a.max_blocks;
-  pp.block_size = a.cache.block_size;
-  pp.num_blocks = a.cache.num_blocks;
-  pp.row_chunks = a.cache.num_kv_heads * D / 8;
-  pp.do_plan = 1;
-  // One CTA plans; with a store (pkv_paged_decode_store) more CTAs copy the new rows, about four
-  // 16-byte chunks of K and of V per thread.
-  int store_ctas = 0;
-  if (a.k_new != nullptr) {
-    const int64_t chunks = (int64_t)a.num_seqs * pp.row_chunks;
-    const int64_t want = (chunks + 4 * kPlanThreads - 1) / (4 * kPlanThreads);
-    store_ctas = (int)(want < num_sms ? want : num_sms);
-    if (store_ctas < 1) store_ctas = 1;
-  }
-  decode_plan_kernel<<<1 + store_ctas, kPlanThreads, 0, stream>>>(pp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_decode_plan(a, p.head_groups, (int32_t)((int64_t)num_sms * ctas_per_sm),
+                                     a.max_splits > 1 ? p.head_groups * T::kWarps : 0,
+                                     p.cap_tokens, num_sms, stream);
   if (e != cudaSuccess) return e;
   // The decode grid is a programmatic dependent of the plan: it is scheduled while the plan runs
   // and waits for it in-kernel, which hides the launch gap between the two.
@@ -1017,6 +985,46 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
 }
 
 }  // namespace
+
+cudaError_t launch_decode_plan(const DecodeArgs& a, int32_t head_groups, int32_t slots,
+                               int32_t counters_per_seq, int32_t cap_tokens, int num_sms,
+                               cudaStream_t stream) {
+  PlanParams pp;
+  pp.context_lens = a.context_lens;
+  pp.items = a.ws.items;
+  pp.header = a.ws.header;
+  pp.counters = a.ws.counters;
+  pp.flags = a.flags;
+  pp.num_seqs = a.num_seqs;
+  pp.cap_tokens = cap_tokens;
+  pp.split_floor = a.split_tokens;
+  pp.fixed_split = a.auto_split ? 0 : a.split_tokens;
+  pp.head_groups = head_groups;
+  pp.slots = slots;
+  pp.counters_per_seq = counters_per_seq;
+  pp.k_new = a.k_new;
+  pp.v_new = a.v_new;
+  pp.slot_mapping = a.slot_mapping;
+  pp.k_cache = const_cast<uint16_t*>(a.k_cache);
+  pp.v_cache = const_cast<uint16_t*>(a.v_cache);
+  pp.block_tables = a.block_tables;
+  pp.max_blocks = a.max_blocks;
+  pp.block_size = a.cache.block_size;
+  pp.num_blocks = a.cache.num_blocks;
+  pp.row_chunks = a.cache.num_kv_heads * a.cache.head_dim / 8;
+  pp.do_plan = 1;
+  // One CTA plans; with a store (pkv_paged_decode_store) more CTAs copy the new rows, about four
+  // 16-byte chunks of K and of V per thread.
+  int store_ctas = 0;
+  if (a.k_new != nullptr) {
+    const int64_t chunks = (int64_t)a.num_seqs * pp.row_chunks;
+    const int64_t want = (chunks + 4 * kPlanThreads - 1) / (4 * kPlanThreads);
+    store_ctas = (int)(want < num_sms ? want : num_sms);
+    if (store_ctas < 1) store_ctas = 1;
+  }
+  decode_plan_kernel<<<1 + store_ctas, kPlanThreads, 0, stream>>>(pp);
+  return cudaGetLastError();
+}
 
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                               int32_t max_splits, DecodeWorkspace* carve, void* base) {

@@ -58,13 +58,24 @@ def test_decode_plan_no_split_for_short_contexts(pk):
     assert plan.workspace_bytes >= 256 + 1024 * 8
 
 
-def test_decode_plan_engine_defaults_to_cuda_core(pk):
-    """pkv_decode_plan_make always picks the CUDA-core engine; the tensor-core one is opt-in."""
+@pytest.mark.parametrize("bs,hkv,d,hq,engine", [
+    (256, 8, 128, 32, "TENSOR_CORE"),   # Qwen3-8B shape
+    (256, 8, 128, 64, "TENSOR_CORE"),   # G = 8
+    (128, 4, 128, 16, "TENSOR_CORE"),
+    (256, 8, 128, 16, "CUDA_CORE"),     # G = 2 (Qwen3-0.6B shape)
+    (256, 8, 128, 8, "CUDA_CORE"),      # G = 1
+    (64, 8, 128, 32, "CUDA_CORE"),      # blocks below 128 rows
+    (16, 8, 128, 32, "CUDA_CORE"),
+    (256, 8, 64, 32, "CUDA_CORE"),      # head_dim 64
+])
+def test_decode_plan_engine_default(pk, bs, hkv, d, hq, engine):
+    """pkv_decode_plan_make picks the tensor-core engine for head_dim 128, block_size >= 128 and
+    G >= 4, else the CUDA-core engine; split settings do not change the choice."""
     plan = pk.DecodePlan()
-    for B, hq, ctx, hint in ((1024, 32, 2048, 0), (1024, 64, 2048, -1), (64, 32, 32768, 0)):
-        assert pk.lib.pkv_decode_plan_make(B, hq, _desc(pk, 5000, 256), ctx, hint,
+    for B, ctx, hint in ((1024, 2048, 0), (1024, 2048, -1), (64, 32768, 0), (8, 100, 256)):
+        assert pk.lib.pkv_decode_plan_make(B, hq, _desc(pk, 5000, bs, hkv, d), ctx, hint,
                                            ctypes.byref(plan)) == 0
-        assert plan.engine == pk.DECODE_ENGINE_CUDA_CORE
+        assert plan.engine == getattr(pk, "DECODE_ENGINE_" + engine)
     assert pk.decode_plan.__defaults__[-1] is None
 
 
@@ -130,8 +141,10 @@ def test_decode_validation_without_launch(pk):
     assert call(Hq=12) == -1
     plan.engine = 7                               # no such engine
     assert call() == -1
-    plan.engine = pk.DECODE_ENGINE_TENSOR_CORE    # group size 2: no tensor-core instance
-    assert call(Hq=16) == -2
+    plan.engine = pk.DECODE_ENGINE_TENSOR_CORE    # head_dim 64: no tensor-core instance
+    d64 = _desc(pk, d=64)
+    assert pk.lib.pkv_paged_decode(256, 256, 256, d64, 256, 8, 256, 4, 32, 0.1, ctypes.byref(plan),
+                                   256, 4096, plan.workspace_bytes, None) == -2
     assert b"tensor-core" in pk.lib.pkv_last_error()
 
 

@@ -274,53 +274,62 @@ def test_decode_graph_capture_matches_eager():
 # ------------------------------------------------------------------------------------------------
 
 
-def _full_size(orc, ctx, Hq, Hkv, D, BS, seed, sample, pad_to=0, split=0):
+ENGINES = [pk.DECODE_ENGINE_CUDA_CORE, pk.DECODE_ENGINE_TENSOR_CORE]
+ENGINE_IDS = ["cuda_core", "tensor_core"]
+
+
+def _full_size(orc, ctx, Hq, Hkv, D, BS, seed, sample, pad_to=0, split=0, engine=None):
     layer = DeviceDecodeLayer(ctx, Hq, Hkv, D, BS, seed, pad_to=pad_to)
     snap = layer.snapshot(sample)
     pk.kv_store(layer.k_new, layer.v_new, layer.slots_dev, layer.k_cache, layer.v_cache)
     out = pk.paged_decode(layer.q, layer.k_cache, layer.v_cache, layer.bt_dev, layer.ctx_dev,
-                          layer.scale, max_context_len=int(ctx.max()), split_tokens=split)
+                          layer.scale, max_context_len=int(ctx.max()), split_tokens=split,
+                          engine=engine)
     assert pk.get_device_error() == 0
     ref, kc_ref, vc_ref = oracle_decode_from_snapshot(orc, snap, layer.scale, Hq)
     idx = torch.from_numpy(snap["blocks"].astype(np.int64)).cuda()
     assert np.array_equal(host_bits(layer.k_cache.index_select(0, idx)), kc_ref)
     assert np.array_equal(host_bits(layer.v_cache.index_select(0, idx)), vc_ref)
     err = assert_attn_close(out[torch.as_tensor(sample, device="cuda")], ref,
-                            what=f"full-size B={len(ctx)} Hq={Hq} BS={BS}")
+                            what=f"full-size B={len(ctx)} Hq={Hq} BS={BS} engine={engine}")
     assert torch.isfinite(out.float()).all()
     return err
 
 
 @pytest.mark.slow
-def test_full_qwen3_8b_decode_layer(orc):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_full_qwen3_8b_decode_layer(orc, engine):
     ctx = W.decode_lengths("qwen3_8b_decode")
     rng = W.rng_for(3, 200)
     sample = np.concatenate([[int(np.argmax(ctx)), int(np.argmin(ctx))],
                              rng.choice(len(ctx), 14, replace=False)])
-    _full_size(orc, ctx, 32, 8, 128, 256, 3, sample)
+    _full_size(orc, ctx, 32, 8, 128, 256, 3, sample, engine=engine)
 
 
 @pytest.mark.slow
-def test_full_qwen3_8b_live_batch_with_ladder_padding(orc):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_full_qwen3_8b_live_batch_with_ladder_padding(orc, engine):
     """A live batch below 1024 padded to the CUDA-graph ladder: padded rows have context 0."""
     n = W.live_batch_size("qwen3_8b_decode")
     live = W.decode_lengths("qwen3_8b_decode", live=n)
     padded = W.ladder_padded_size(n)
     ctx = np.concatenate([live, np.zeros(padded - n, np.int32)])
     sample = np.concatenate([np.arange(3), [n - 1, n, padded - 1]])
-    _full_size(orc, ctx, 32, 8, 128, 256, 13, sample, pad_to=padded)
+    _full_size(orc, ctx, 32, 8, 128, 256, 13, sample, pad_to=padded, engine=engine)
 
 
 @pytest.mark.slow
-def test_full_qwen3_0p6b_decode_layer(orc):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_full_qwen3_0p6b_decode_layer(orc, engine):
     ctx = W.decode_lengths("qwen3_0p6b_decode")
     sample = W.rng_for(2, 200).choice(len(ctx), 16, replace=False)
-    _full_size(orc, ctx, 16, 8, 128, 256, 2, sample)
+    _full_size(orc, ctx, 16, 8, 128, 256, 2, sample, engine=engine)
 
 
 @pytest.mark.slow
-def test_full_long_context_split_decode(orc):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_full_long_context_split_decode(orc, engine):
     ctx = W.decode_lengths("long_splitk_decode")
     sample = np.concatenate([[0, 3], np.arange(4, 64, 3)])
     for split in (0, 256):
-        _full_size(orc, ctx, 32, 8, 128, 16, 5, sample, split=split)
+        _full_size(orc, ctx, 32, 8, 128, 16, 5, sample, split=split, engine=engine)

@@ -1,5 +1,6 @@
-"""GPU parity: decode on the tensor-core engine (the tcgen05 attention kernel with one query row
-per sequence) through the C ABI against the fp64 oracle, and against the CUDA-core engine.
+"""GPU parity: decode on the tensor-core engine (tcgen05 MMAs with 128 keys on the M dimension
+and a kv head's query heads on N) through the C ABI against the fp64 oracle, and against the
+CUDA-core engine.
 
 Bars as for the CUDA-core engine: outputs within max-abs 2e-2 of the oracle on N(0,1) inputs,
 exactly bf16(V0) for a one-token context, zeros for a padded (context 0) row, and the store of a
@@ -48,13 +49,16 @@ def _oracle(orc, case):
     return orc.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale)
 
 
-TC_SHAPES = [  # (B, Hq, Hkv, BS, ctx_lo, ctx_hi): head_dim 128, group size 4 or 8
+TC_SHAPES = [  # (B, Hq, Hkv, BS, ctx_lo, ctx_hi): head_dim 128, group sizes 1, 2, 4 and 8
     (6, 32, 8, 256, 100, 900),
     (9, 32, 8, 16, 1, 700),
     (5, 64, 8, 32, 1, 500),
     (7, 16, 4, 64, 30, 1300),
     (4, 32, 4, 128, 60, 1100),
     (3, 8, 1, 16, 1, 4000),
+    (8, 16, 8, 256, 1, 1024),
+    (5, 8, 8, 64, 100, 2000),
+    (6, 4, 2, 128, 1, 3000),
 ]
 
 
@@ -70,11 +74,23 @@ def test_tc_decode_shapes(orc, shape, q_scale):
     assert (out.float() - cc.float()).abs().max().item() <= TOL
 
 
+@pytest.mark.parametrize("split", [128, 256, 512, -1, 0], ids=lambda s: f"split{s}")
+@pytest.mark.parametrize("hq", [32, 16, 64], ids=lambda h: f"Hq{h}")
+def test_tc_decode_split(orc, split, hq):
+    """Chunked contexts (flash-decoding split) merged in the kernel: against the oracle, and the
+    split result against the unsplit one."""
+    case = W.random_decode_case(4050 + hq, 7, hq, 8, 128, 16, 1, 3000, extra_pool=2)
+    out, d = _decode(case, TC, split_tokens=split)
+    assert_attn_close(out, _oracle(orc, case), what=f"tensor-core split={split} Hq={hq}")
+    whole, _ = _decode(case, TC, split_tokens=-1, stored=d)
+    assert (out.float() - whole.float()).abs().max().item() <= TOL
+
+
 def test_tc_decode_ragged_edges(orc):
-    """Contexts at and around the 64-key tile and block boundaries, and a single token."""
+    """Contexts at and around the 128-key tile and block boundaries, and a single token."""
     ctx = np.array([1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512, 513],
                    np.int32)
-    for Hq, BS in ((32, 16), (64, 256), (32, 64)):
+    for Hq, BS in ((32, 16), (64, 256), (32, 64), (16, 128), (8, 32)):
         case = W.random_decode_case(4100 + Hq + BS, len(ctx), Hq, 8, 128, BS, 0, 0,
                                     context_lens=ctx)
         out, _ = _decode(case, TC)
