@@ -142,11 +142,6 @@ struct PrefillArgs {
   uint16_t* out;
   int* flags;
   int32_t* item_counter;  // device, in the caller's workspace
-  // Decode on the tensor cores (cu_seqlens_q / cu_seqlens_k unused) when non-null: sequence b
-  // has the single query row b of q [num_seqs, num_q_heads, 128] and context_lens[b] cached keys
-  // (clamped to cap_tokens); max_seqlen_q is 1 and total_q is num_seqs.
-  const int32_t* context_lens = nullptr;
-  int32_t cap_tokens = 0;
   // Dense item numbering (nullptr: ids run over num_seqs x num_kv_heads x ceil(max_seqlen_q /
   // positions per tile), and the grid skips the ids of query tiles a sequence does not have):
   // num_seqs + 1 ints in the caller's workspace, which a one-CTA plan kernel fills with each

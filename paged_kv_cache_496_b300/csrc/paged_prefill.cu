@@ -94,10 +94,6 @@ struct PrefillParams {
   int32_t box_rows;      // rows per K/V TMA box
   int32_t oob_row;       // a row coordinate past the end of the K/V tensors (zero fill)
   float qk_scale_log2;
-  // Decode (one query row per sequence; cu_q and cu_k unused) when non-null: sequence b has
-  // q row b and context_lens[b] keys, clamped to cap_tokens; context 0 gives zeros.
-  const int32_t* context_lens;
-  int32_t cap_tokens;
   // Dense numbering when non-null: the items of sequence b are ids item_prefix[b] ..
   // item_prefix[b + 1] - 1 (its kv heads x its own query tiles), item_prefix[num_seqs] of them
   // in all; written by prefill_plan_kernel before this grid reads them.
@@ -117,7 +113,6 @@ static_assert(sizeof(Item) / 4 + 1 <= kItemInts, "item slot size");
 
 constexpr int kItemSkip = 0;  // no work (a tile past the sequence's end, or invalid lengths)
 constexpr int kItemWork = 1;
-constexpr int kItemZero = 2;  // decode of a sequence with context 0: its output rows are zeros
 
 // Items are numbered so that the query tiles of one (sequence, kv head) are adjacent, longest
 // first: CTAs that run at the same time then share that head's K/V through L2. Invalid lengths
@@ -148,22 +143,9 @@ __device__ __forceinline__ int load_item(const PrefillParams& p, int id, Item& i
   const int t = id / p.num_q_tiles;
   it.g = t % p.num_kv_heads;
   it.b = t / p.num_kv_heads;
-  if (p.context_lens != nullptr) {
-    // decode: query row b attends to all of its context_lens[b] cached keys
-    int ctx = __ldg(p.context_lens + it.b);
-    if (ctx > p.cap_tokens) {
-      if (it.g == 0) raise_flag(p.flags, PKV_DEVERR_CTX_CLAMPED);
-      ctx = p.cap_tokens;
-    }
-    if (ctx <= 0) return kItemZero;
-    it.q_start = it.b;
-    it.q_len = 1;
-    it.k_len = ctx;
-  } else {
-    it.q_start = __ldg(p.cu_q + it.b);
-    it.q_len = __ldg(p.cu_q + it.b + 1) - it.q_start;
-    it.k_len = __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
-  }
+  it.q_start = __ldg(p.cu_q + it.b);
+  it.q_len = __ldg(p.cu_q + it.b + 1) - it.q_start;
+  it.k_len = __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
   if (it.q_len < 0 || it.k_len < it.q_len) {
     if (threadIdx.x == 0 && qt == 0 && it.g == 0) raise_flag(p.flags, PKV_DEVERR_BAD_LENGTHS);
     return kItemSkip;
@@ -174,14 +156,6 @@ __device__ __forceinline__ int load_item(const PrefillParams& p, int id, Item& i
   const int last_pos = min(it.q_len, it.q0 + p.pos_per_tile) - 1;
   it.n_kt = (it.P + last_pos + 1 + kKeys - 1) / kKeys;
   return kItemWork;
-}
-
-// Decode of a sequence with context 0 (a padded batch entry): zeros for the G query heads of kv
-// head it.g, written by the producer thread that claimed the item.
-__device__ __forceinline__ void write_zero_rows(const PrefillParams& p, const Item& it) {
-  uint4* dst = reinterpret_cast<uint4*>(
-      p.out + ((int64_t)it.b * p.num_q_heads + it.g * p.group) * kHD);
-  for (int i = 0; i < p.group * kHD / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Persistent: the producer claims item ids in increasing order from a global counter (skipping
@@ -342,12 +316,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
         while (claimed < num_items) {
           const int c = claimed;
           claimed = atomicAdd(p.item_counter, 1);
-          const int kind = load_item(p, c, it);
-          if (kind == kItemWork) {
+          if (load_item(p, c, it) == kItemWork) {
             id = c;
             break;
           }
-          if (kind == kItemZero) write_zero_rows(p, it);
         }
         ok = mbar_wait(bar(kBarItemEmpty + (n & 1)), ((n >> 1) & 1) ^ 1);
         if (ok) {
@@ -805,8 +777,6 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
   p.box_rows = prefill_kv_box_rows(a.cache.block_size, paged);
   p.oob_row = paged ? a.cache.num_blocks * a.cache.block_size : a.total_q;
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
-  p.context_lens = a.context_lens;
-  p.cap_tokens = a.cap_tokens;
   p.item_prefix = a.item_prefix;
   // upper bound of the item count (the exact count, with dense numbering, is on the device)
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads * a.num_seqs;
