@@ -161,8 +161,9 @@ def kv_store(k, v, slot_mapping, k_cache, v_cache, stream=None):
 def decode_plan(num_seqs: int, num_q_heads: int, k_cache: torch.Tensor, max_context_len: int,
                 split_tokens: int = 0, engine: Optional[int] = None) -> DecodePlan:
     """Host-side decode plan (chunking, workspace size and engine); see pkv_decode_plan_make.
-    engine: None keeps the library's choice, else DECODE_ENGINE_CUDA_CORE or
-    DECODE_ENGINE_TENSOR_CORE."""
+    engine: None keeps the library's choice (the tensor-core engine for head_dim 128,
+    block_size >= 128 and >= 4 query heads per kv head, else the CUDA-core engine), or
+    DECODE_ENGINE_CUDA_CORE / DECODE_ENGINE_TENSOR_CORE to override it."""
     plan = DecodePlan()
     _check(lib.pkv_decode_plan_make(num_seqs, num_q_heads, _cache_desc(k_cache),
                                     int(max_context_len), int(split_tokens), ctypes.byref(plan)))
