@@ -4,8 +4,9 @@
 Default workload: Qwen3-8B-shaped decode -- 1024 sequences, context = input U{100..1024} +
 generated U{100..1024}, 32 query / 8 KV heads, head_dim 128, block_size 256, 36 layer caches with
 random physical block placement. One step = for each of the 36 layers: the store of the newest
-token of every sequence and paged decode attention over the whole context, as one
-pkv_paged_decode_store call (--unfused: pkv_kv_store, then pkv_paged_decode).
+token of every sequence (pkv_kv_store) and paged decode attention over the whole context
+(pkv_paged_decode); the first layer's decode call plans on the device and the later ones reuse
+that plan (--replan: every layer plans; --fused: one pkv_paged_decode_store per layer).
 
 Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle on a bounded sample of
 the same workload instead (the only reference implementation of this path).
@@ -183,7 +184,7 @@ class DecodeStep:
     """All layers of one decode step, resident in HBM."""
 
     def __init__(self, name, torch, pk, device, log_fill=True, num_seqs=None, num_layers=None,
-                 fused=False, engine=None):
+                 fused=False, engine=None, reuse_plan=True):
         self.w = w = W.WORKLOADS[name]
         self.torch, self.pk = torch, pk
         self.ctx = W.decode_lengths(name)
@@ -226,8 +227,12 @@ class DecodeStep:
                               device=device)
         self.kv_bytes_per_layer = int(self.ctx.sum()) * w.kv_bytes_per_token
         self.fused = fused
-        # per layer: (store,) decode plan, decode
-        self.launches_per_step = (2 if fused else 3) * self.L
+        # Layers after the first run on the device plan the first one wrote (same lengths): with
+        # the store fused, every layer launches the plan-or-store grid and the decode kernel;
+        # without, kv_store and the decode kernel, plus the first layer's plan kernel.
+        self.reuse = reuse_plan
+        self.launches_per_step = (2 * self.L if fused else
+                                  (2 * self.L + 1 if reuse_plan else 3 * self.L))
 
     def layer(self, l, pre=None, post=None):
         """Store the newest token of every sequence and decode layer l."""
@@ -237,13 +242,15 @@ class DecodeStep:
             pk.kv_store(self.k_new[l], self.v_new[l], self.slots_dev, kc, vc)
         if pre is not None:
             pre.record()
+        reuse = self.reuse and l > 0
         if self.fused:
             pk.paged_decode_store(self.q[l], self.k_new[l], self.v_new[l], self.slots_dev, kc, vc,
                                   self.bt_dev, self.ctx_dev, self.scale, out=self.out[l],
-                                  plan=self.plan, workspace=self.ws)
+                                  plan=self.plan, workspace=self.ws, reuse_plan=reuse)
         else:
             pk.paged_decode(self.q[l], kc, vc, self.bt_dev, self.ctx_dev, self.scale,
-                            out=self.out[l], plan=self.plan, workspace=self.ws)
+                            out=self.out[l], plan=self.plan, workspace=self.ws,
+                            reuse_plan=reuse)
         if post is not None:
             post.record()
 
@@ -463,15 +470,18 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
-    ap.add_argument("--unfused", action="store_true",
-                    help="pkv_kv_store then pkv_paged_decode per layer instead of one "
-                         "pkv_paged_decode_store (the step's store fused into the decode call)")
+    ap.add_argument("--fused", action="store_true",
+                    help="one pkv_paged_decode_store per layer (the step's store in the decode "
+                         "call's first grid) instead of pkv_kv_store then pkv_paged_decode")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload (not a bench number)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling only: the first N sequences (not a bench number)")
     ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"],
                     help="decode engine (auto: the library's choice for the shape)")
+    ap.add_argument("--replan", action="store_true",
+                    help="plan on the device in every layer's decode call instead of reusing the "
+                         "first layer's plan")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -500,7 +510,8 @@ def main():
     engine = {"auto": None, "cuda_core": pk.DECODE_ENGINE_CUDA_CORE,
               "tensor_core": pk.DECODE_ENGINE_TENSOR_CORE}[args.engine]
     step = DecodeStep(args.workload, torch, pk, device, num_seqs=args.num_seqs,
-                      num_layers=args.layers, fused=not args.unfused, engine=engine)
+                      num_layers=args.layers, fused=args.fused, engine=engine,
+                      reuse_plan=not args.replan)
     engine_name = decode_engine_name(pk, step.plan.engine)
     reduced = bool(args.num_seqs or args.layers)
     w = step.w
@@ -517,8 +528,12 @@ def main():
         step.run()
     torch.cuda.synchronize()
     assert pk.get_device_error() == 0, "device error flag raised during warm-up"
+    # CUDA events around every decode call of every fifth timed step (and of the last one): an
+    # event between two kernels costs the stream a few microseconds, so bracketing every call
+    # of every step would slow the step being measured by ~0.5-0.9%.
+    sampled = [i % 5 == 4 or i == args.steps - 1 for i in range(args.steps)]
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(step.L)]
-           for _ in range(args.steps)]
+           if sampled[i] else None for i in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -530,7 +545,7 @@ def main():
         torch.cuda.synchronize()
     barrier()
     ms = ranks_max(start.elapsed_time(stop) / args.steps)
-    decode_ms = [e[0].elapsed_time(e[1]) for s in evs for e in s]
+    decode_ms = [e[0].elapsed_time(e[1]) for s in evs if s is not None for e in s]
     decode_ms_mean = ranks_max(sum(decode_ms) / len(decode_ms))
     flags = pk.get_device_error()
     if flags:
@@ -625,10 +640,12 @@ def main():
                        "mean_context": float(step.ctx.mean()),
                        "kv_bytes_per_step": kv_step, "distinct_layer_pools": step.n_pools,
                        "l2": "inputs larger than L2 (KV read per layer >> 126 MB), no flush",
-                       "step": ("per layer: one pkv_paged_decode_store (the plan grid also "
-                                "stores the newest token of every sequence; then the persistent "
-                                "decode kernel)" if step.fused else
-                                "per layer: kv_store (1 token/seq), then paged_decode"),
+                       "step": ("per layer: one pkv_paged_decode_store (a grid that stores the "
+                                "newest token of every sequence and, in the first layer, plans; "
+                                "then the persistent decode kernel)" if step.fused else
+                                "per layer: kv_store (1 token/seq), then paged_decode") +
+                               ("; layers after the first reuse the first layer's device plan"
+                                if step.reuse else "; every layer plans"),
                        "decode_engine": engine_name,
                        "parallelism": f"replicas x{world}",
                        "reduced_for_profiling": reduced},
@@ -639,7 +656,10 @@ def main():
                                       "paged_decode_tc_kernel" if engine_name == "tensor_core"
                                       else "paged_decode_kernel"),
                          "algorithmic_bytes_per_launch": step.kv_bytes_per_layer,
-                         "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind},
+                         "mean_launch_ms": decode_ms_mean, "peak_source": peak_kind,
+                         "decode_calls_timed": len(decode_ms),
+                         "timed_calls": "every decode call of every fifth timed step and of the "
+                                        "last one, CUDA events on the launching stream"},
             "clocks": clocks.summary(),
             "gpu_launches": step.launches_per_step * args.steps,
             "device_error_flags": flags,
@@ -676,6 +696,14 @@ def secondary_measurements(torch, pk, device, main_step):
     ms = timed(main_step.run, reps=3)
     main_step.fused = was
     res["fused_step" if not was else "unfused_step"] = {
+        "ms": ms, "GB/s": main_step.kv_bytes_per_layer * main_step.L / ms / 1e6}
+
+    # the same step planning in every layer instead of reusing the first layer's device plan
+    was = main_step.reuse
+    main_step.reuse = not was
+    ms = timed(main_step.run, reps=3)
+    main_step.reuse = was
+    res["step_planning_every_layer" if was else "step_reusing_plan"] = {
         "ms": ms, "GB/s": main_step.kv_bytes_per_layer * main_step.L / ms / 1e6}
 
     # the same step on the other decode engine (the library picks one per shape)

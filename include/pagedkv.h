@@ -115,6 +115,24 @@ PKV_API int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* sl
 #define PKV_DECODE_ENGINE_CUDA_CORE 1
 #define PKV_DECODE_ENGINE_TENSOR_CORE 2
 
+/*
+ * flags (0 from pkv_decode_plan_make; the caller may set):
+ *   PKV_DECODE_PLAN_REUSE  the decode call launches no plan kernel and runs on the device plan
+ *                          (chunk length, work list) already in its workspace. Valid when the
+ *                          previous decode call on that workspace used this plan, the same
+ *                          num_seqs, num_q_heads and cache geometry, and context_lens with the
+ *                          same values, e.g. every layer of a decode step after the first, as
+ *                          the per-step attention metadata of ["nano-vllm 深度分析报告", table
+ *                          "可复用的模式与技巧"] is set once per step. Every decode call leaves
+ *                          its workspace's work counters reset for such a call. With
+ *                          pkv_paged_decode_store the step's store still runs, in a grid of
+ *                          its own before the decode kernel. A reuse that breaks these
+ *                          conditions gives wrong outputs for the sequences whose lengths
+ *                          changed (never an access outside the caches or the workspace:
+ *                          every table entry and context is still bounds-checked).
+ */
+#define PKV_DECODE_PLAN_REUSE 1
+
 typedef struct pkv_decode_plan {
   int32_t split_tokens;
   int32_t max_splits;
@@ -122,7 +140,7 @@ typedef struct pkv_decode_plan {
   int32_t max_context_len;
   size_t workspace_bytes;
   int32_t engine;
-  int32_t reserved;
+  int32_t flags;
 } pkv_decode_plan;
 
 PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc cache,
@@ -148,7 +166,8 @@ PKV_API int pkv_decode_plan_make(int32_t num_seqs, int32_t num_q_heads, pkv_cach
  *                 the caller. Every call rewrites it, so calls that share one workspace must be
  *                 ordered on one stream.
  * Launches: a one-CTA plan kernel (chunking, work list) and the persistent decode kernel of the
- * plan's engine, launched as its programmatic dependent.
+ * plan's engine, launched as its programmatic dependent; with PKV_DECODE_PLAN_REUSE in
+ * plan->flags, the decode kernel alone.
  */
 PKV_API int pkv_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                      pkv_cache_desc cache, const int32_t* block_tables,
@@ -237,9 +256,11 @@ PKV_API int pkv_paged_decode_static_ws(const uint16_t* q, const uint16_t* k_cach
  * pkv_paged_decode(...) when, as in a decode step, slot_mapping[b] is the slot of position
  * context_lens[b] - 1 of sequence b (or -1 for a padded entry with context 0):
  *   - k_new[b], v_new[b] are written to slot_mapping[b] (skipped when -1) by the call's first
- *     grid (with the CUDA-core engine the same grid also plans the attention work); the
- *     attention grid starts once that grid is complete and reads all ctx positions from the
- *     cache, so the result equals store-then-decode bit for bit, with one launch fewer;
+ *     grid, which also plans the attention work unless the plan is reused; the attention grid
+ *     starts once that grid is complete and reads all ctx positions from the cache, so the
+ *     result equals store-then-decode bit for bit, with one launch fewer than store, plan and
+ *     decode. (With a reused plan, pkv_kv_store then pkv_paged_decode measured ~0.4% faster on
+ *     a B300: this call's store also checks every slot against the block table.)
  *   - a slot outside the cache is skipped and raises PKV_DEVERR_BAD_SLOT; a slot that is not
  *     the block table's slot of position ctx-1 (or any slot other than -1 for a sequence of
  *     context 0) is still written and raises PKV_DEVERR_BAD_SLOT; the output row of that
@@ -328,7 +349,7 @@ PKV_API const char* pkv_status_string(int status);
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version: major * 10000 + minor * 100 + patch. 0.2.0 added the prefill workspace. */
-#define PKV_VERSION 201
+#define PKV_VERSION 202
 PKV_API int pkv_version(void);
 
 #ifdef __cplusplus

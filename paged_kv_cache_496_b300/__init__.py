@@ -41,6 +41,7 @@ DEVERR_BAD_LENGTHS = 16
 
 DECODE_ENGINE_CUDA_CORE = 1    # PKV_DECODE_ENGINE_CUDA_CORE
 DECODE_ENGINE_TENSOR_CORE = 2  # PKV_DECODE_ENGINE_TENSOR_CORE
+DECODE_PLAN_REUSE = 1          # PKV_DECODE_PLAN_REUSE
 
 
 class CacheDesc(ctypes.Structure):
@@ -52,7 +53,7 @@ class DecodePlan(ctypes.Structure):
     _fields_ = [("split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("auto_split", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t), ("engine", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -61,7 +62,7 @@ class PagedKVError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 201  # PKV_VERSION of include/pagedkv.h that the argtypes below describe
+ABI_VERSION = 202  # PKV_VERSION of include/pagedkv.h that the argtypes below describe
 
 
 def _load():
@@ -202,14 +203,25 @@ def workspace_for(plan: DecodePlan, device: torch.device, stream=None) -> torch.
         return ws
 
 
+def _reused(plan: Optional[DecodePlan]) -> DecodePlan:
+    """A copy of plan with PKV_DECODE_PLAN_REUSE set (the caller's plan object is unchanged)."""
+    if plan is None:
+        raise ValueError("reuse_plan needs the plan of the earlier decode call")
+    p = DecodePlan.from_buffer_copy(plan)
+    p.flags |= DECODE_PLAN_REUSE
+    return p
+
+
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
                  max_context_len: Optional[int] = None, split_tokens: int = 0,
                  plan: Optional[DecodePlan] = None, workspace: Optional[torch.Tensor] = None,
-                 stream=None, engine: Optional[int] = None):
+                 stream=None, engine: Optional[int] = None, reuse_plan: bool = False):
     """Decode attention over the paged cache. Returns out [num_seqs, num_q_heads, head_dim] bf16.
 
     max_context_len bounds context_lens (host int); if omitted it is read from the device (a
     synchronisation). split_tokens: 0 automatic, > 0 fixed chunk length, < 0 never split.
+    reuse_plan: run on the device plan the previous call with this plan and workspace left
+    (same lengths, e.g. the layers of a decode step after the first): no plan kernel.
     """
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
@@ -232,6 +244,8 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
         plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens, engine)
     if workspace is None:
         workspace = workspace_for(plan, q.device, stream)
+    if reuse_plan:
+        plan = _reused(plan)
     _check(lib.pkv_paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                 _cache_desc(k_cache), block_tables.data_ptr(),
                                 block_tables.shape[1], context_lens.data_ptr(), B, Hq,
@@ -244,9 +258,10 @@ def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_ta
                        context_lens, scale: float, out=None, max_context_len: Optional[int] = None,
                        split_tokens: int = 0, plan: Optional[DecodePlan] = None,
                        workspace: Optional[torch.Tensor] = None, stream=None,
-                       engine: Optional[int] = None):
+                       engine: Optional[int] = None, reuse_plan: bool = False):
     """One decode step with the store fused in: writes k_new[b], v_new[b] to slot_mapping[b] and
-    attends over context_lens[b] tokens, the last of which is taken from k_new / v_new."""
+    attends over context_lens[b] tokens, the last of which is taken from k_new / v_new.
+    reuse_plan as for paged_decode (the store still runs, in a grid of its own)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_new, "k_new", torch.bfloat16, 3)
     _need(v_new, "v_new", torch.bfloat16, 3)
@@ -267,6 +282,8 @@ def paged_decode_store(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_ta
         plan = decode_plan(B, Hq, k_cache, max_context_len, split_tokens, engine)
     if workspace is None:
         workspace = workspace_for(plan, q.device, stream)
+    if reuse_plan:
+        plan = _reused(plan)
     _check(lib.pkv_paged_decode_store(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                                       slot_mapping.data_ptr(), k_cache.data_ptr(),
                                       v_cache.data_ptr(), _cache_desc(k_cache),

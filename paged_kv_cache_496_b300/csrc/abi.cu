@@ -395,6 +395,8 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
     return fail(PKV_ERR_INVALID_ARG, "malformed decode plan");
   if (plan->engine != PKV_DECODE_ENGINE_CUDA_CORE && plan->engine != PKV_DECODE_ENGINE_TENSOR_CORE)
     return fail(PKV_ERR_INVALID_ARG, "decode plan engine %d", plan->engine);
+  if ((plan->flags & ~PKV_DECODE_PLAN_REUSE) != 0)
+    return fail(PKV_ERR_INVALID_ARG, "decode plan flags %#x", (unsigned)plan->flags);
   const int G = num_q_heads / cache.num_kv_heads;
   const bool tc = plan->engine == PKV_DECODE_ENGINE_TENSOR_CORE;
   if (tc && cache.head_dim != 128)
@@ -438,6 +440,7 @@ static int decode_impl(const uint16_t* q, const uint16_t* k_cache, const uint16_
   a.v_new = v_new;
   a.slot_mapping = slot_mapping;
   a.ctas_per_sm = d->decode_ctas;
+  a.reuse_plan = (plan->flags & PKV_DECODE_PLAN_REUSE) != 0;
   const int64_t rows = (int64_t)cache.num_blocks * cache.block_size;
   CUtensorMap tk, tv;
   cudaError_t e = cudaSuccess;

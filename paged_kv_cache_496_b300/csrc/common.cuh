@@ -44,6 +44,18 @@ __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Decode work counters in the workspace header: [0] claim counter, [3] producers done. The
+// producer warp of every CTA calls this once, after its last claim; the last one resets both, so
+// the next decode call on the same workspace can run on the same device plan without a plan
+// kernel. Only producers claim, and a producer's claims are performed before it counts itself out.
+__device__ __forceinline__ void release_claims(uint32_t* header) {
+  __threadfence();
+  if (atomicAdd(header + 3, 1u) == gridDim.x - 1) {
+    atomicExch(header, 0u);
+    atomicExch(header + 3, 0u);
+  }
+}
+
 __device__ __forceinline__ void raise_flag(int* flags, int bit) {
   if (flags != nullptr) atomicOr(flags, bit);
 }

@@ -84,6 +84,9 @@ struct DecodeArgs {
   const uint16_t* v_new = nullptr;
   const int32_t* slot_mapping = nullptr;
   const int* ctas_per_sm = nullptr;  // ContextState::decode_ctas of the current context
+  // The workspace holds the device plan of an earlier call with the same plan and lengths: no
+  // plan kernel (with a store, a store-only grid runs before the decode kernel instead).
+  bool reuse_plan = false;
 };
 
 // Whole-block moves: mode 0 copies (src, dst) pairs inside the caches, mode 1 gathers blocks

@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanPar
   if (tid == 0) {
     pp.header[1] = total;  // number of (sequence, chunk) items
     pp.header[0] = 0u;     // claim counter
+    pp.header[3] = 0u;     // producers done (release_claims)
   }
 }
 
@@ -581,6 +582,7 @@ __global__ void __maxnreg__(168)
       c = c_next;
     }
     if (!ok && lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) release_claims(p.header);
     // Drain: never leave while a copy into this CTA's shared memory may be in flight.
     if (lane == 0) {
       const uint32_t n = issue < (uint32_t)T::kStages ? issue : (uint32_t)T::kStages;
@@ -891,14 +893,14 @@ __global__ void __maxnreg__(168)
       // slice) merges all chunks: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
       __threadfence();
       __syncwarp();
+      uint32_t* ctr = p.counters + ((int64_t)mt.b * p.head_groups + mt.x) * T::kWarps + warp;
       uint32_t done = 0;
-      if (lane == 0)
-        done = atomicAdd(p.counters + ((int64_t)mt.b * p.head_groups + mt.x) * T::kWarps + warp,
-                         1u);
+      if (lane == 0) done = atomicAdd(ctr, 1u);
       done = __shfl_sync(kFullMask, done, 0);
       if (done == (uint32_t)mt.nsplit - 1) {
         __threadfence();
         merge_chunks<D, GH, T::kWarps>(p, mt.b, mt.x, mt.nsplit, warp, lane);
+        if (lane == 0) *ctr = 0u;  // all chunks counted: ready for the next call
       }
     }
     ++item;
@@ -965,9 +967,12 @@ cudaError_t launch_instance(const DecodeArgs& a, const CUtensorMap& tk, const CU
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
 
-  cudaError_t e = launch_decode_plan(a, p.head_groups, (int32_t)((int64_t)num_sms * ctas_per_sm),
-                                     a.max_splits > 1 ? p.head_groups * T::kWarps : 0,
-                                     p.cap_tokens, num_sms, stream);
+  cudaError_t e =
+      a.reuse_plan ? (a.k_new != nullptr ? launch_decode_store_rows(a, num_sms, stream)
+                                         : cudaSuccess)
+                   : launch_decode_plan(a, p.head_groups, (int32_t)((int64_t)num_sms * ctas_per_sm),
+                                        a.max_splits > 1 ? p.head_groups * T::kWarps : 0,
+                                        p.cap_tokens, num_sms, stream);
   if (e != cudaSuccess) return e;
   // The decode grid is a programmatic dependent of the plan: it is scheduled while the plan runs
   // and waits for it in-kernel, which hides the launch gap between the two.

@@ -348,6 +348,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       w_hi = w_hi_nx;
     }
     if (!ok && lane == 0) raise_flag(p.flags, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) release_claims(p.header);  // after the claim issued one item ahead
     // Drain: never leave while a copy into this CTA's shared memory may be in flight.
     if (lane == 0) {
       const uint32_t n = issue < (uint32_t)kStagesT ? issue : (uint32_t)kStagesT;
@@ -598,9 +599,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           // them: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
           __threadfence();
           __syncwarp();
+          uint32_t* ctr = p.counters + ((int64_t)m.b * nkv + m.x) * 4 + quarter;
           uint32_t done = 0;
-          if (lane == 0)
-            done = atomicAdd(p.counters + ((int64_t)m.b * nkv + m.x) * 4 + quarter, 1u);
+          if (lane == 0) done = atomicAdd(ctr, 1u);
           done = __shfl_sync(kFullMask, done, 0);
           if (done == (uint32_t)m.nsplit - 1) {
             __threadfence();
@@ -641,6 +642,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
               p.out[((int64_t)m.b * p.num_q_heads + head0 + h) * kDT + row] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(num * inv));
             }
+            if (lane == 0) *ctr = 0u;  // all chunks counted: ready for the next call
           }
         }
       }
@@ -734,8 +736,11 @@ cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& tq,
   // Chunks are sized as for two CTAs per SM although one runs: with one CTA per SM a chunk of
   // 0.4 of its share leaves a coarse tail (4 x 32768 + 60 short sequences at block_size 256:
   // 5064 GB/s, against 5147 with this sizing and 4332 with four CTAs' sizing).
-  cudaError_t e = launch_decode_plan(a, nkv, 2 * num_sms, a.max_splits > 1 ? nkv * 4 : 0,
-                                     p.cap_tokens, num_sms, stream);
+  cudaError_t e =
+      a.reuse_plan ? (a.k_new != nullptr ? launch_decode_store_rows(a, num_sms, stream)
+                                         : cudaSuccess)
+                   : launch_decode_plan(a, nkv, 2 * num_sms, a.max_splits > 1 ? nkv * 4 : 0,
+                                        p.cap_tokens, num_sms, stream);
   if (e != cudaSuccess) return e;
   switch (G) {
     case 1: return launch_tc_instance<1>(p, (int)grid, tq, tk, tv, tail, stream);

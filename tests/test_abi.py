@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(pk):
 
 
 def test_status_strings_and_version(pk):
-    assert pk.lib.pkv_version() == pk.ABI_VERSION == 201
+    assert pk.lib.pkv_version() == pk.ABI_VERSION == 202
     assert pk.lib.pkv_status_string(0) == b"ok"
     assert pk.lib.pkv_status_string(-3) == b"workspace too small"
     assert pk.lib.pkv_status_string(12345) == b"unknown status"
