@@ -571,48 +571,83 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_bt, h_ctx, h_sl])
         d2h = sum(x.numel() * x.element_size() for x in h_out)
 
-        # Copies overlap compute: layer l's inputs are copied in on one stream while earlier
-        # layers compute, and layer l's output is copied out on another as soon as it is done.
+        # Copies overlap compute, in groups of 6 layers pipelined across steps: group g of step
+        # i + 1 is copied in (stream s_in) as soon as step i has finished with group g, and group
+        # g's outputs are copied out (stream s_out) as soon as they are done. The small per-step
+        # tensors (tables, lengths, slots), which every layer reads, alternate between two sets.
         main = torch.cuda.current_stream()
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(step.L)]
-        ev_done = [torch.cuda.Event() for _ in range(step.L)]
+        groups = [list(range(g, min(g + 6, step.L))) for g in range(0, step.L, 6)]
+        small = [{"bt_dev": step.bt_dev, "ctx_dev": step.ctx_dev, "slots_dev": step.slots_dev},
+                 {n: torch.empty_like(getattr(step, n))
+                  for n in ("bt_dev", "ctx_dev", "slots_dev")}]
+        ev_in = [torch.cuda.Event() for _ in groups]
+        ev_done = [torch.cuda.Event() for _ in groups]
+        ev_out = [torch.cuda.Event() for _ in groups]
+        ev_step = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            s_in.wait_stream(main)  # buffers of the previous step are no longer in use
+        def copy_small(i):  # step i's tables, lengths and slots into set i % 2
+            k = i % 2
             with torch.cuda.stream(s_in):
-                step.bt_dev.copy_(h_bt, non_blocking=True)
-                step.ctx_dev.copy_(h_ctx, non_blocking=True)
-                step.slots_dev.copy_(h_sl, non_blocking=True)
-                for l in range(step.L):
+                if i >= 2:
+                    s_in.wait_event(ev_step[k])  # step i - 2 no longer reads this set
+                small[k]["bt_dev"].copy_(h_bt, non_blocking=True)
+                small[k]["ctx_dev"].copy_(h_ctx, non_blocking=True)
+                small[k]["slots_dev"].copy_(h_sl, non_blocking=True)
+
+        def copy_group(i, g):  # step i's q, k_new, v_new of group g
+            with torch.cuda.stream(s_in):
+                if i >= 1:
+                    s_in.wait_event(ev_done[g])  # step i - 1 has finished group g
+                for l in groups[g]:
                     step.q[l].copy_(h_q[l], non_blocking=True)
                     step.k_new[l].copy_(h_k[l], non_blocking=True)
                     step.v_new[l].copy_(h_v[l], non_blocking=True)
-                    ev_in[l].record(s_in)
-            for l in range(step.L):
-                main.wait_event(ev_in[l])
-                step.layer(l)
-                ev_done[l].record(main)
-                s_out.wait_event(ev_done[l])
-                with torch.cuda.stream(s_out):
-                    h_out[l].copy_(step.out[l], non_blocking=True)
-            main.wait_stream(s_out)
+                ev_in[g].record(s_in)
 
-        for _ in range(args.warmup):
-            e2e_step()
+        def e2e_steps(n):
+            s_in.wait_stream(main)
+            copy_small(0)
+            for g in range(len(groups)):
+                copy_group(0, g)
+            for i in range(n):
+                for name, t in small[i % 2].items():
+                    setattr(step, name, t)
+                if i + 1 < n:
+                    copy_small(i + 1)
+                for g in range(len(groups)):
+                    main.wait_event(ev_in[g])
+                    if i >= 1:
+                        main.wait_event(ev_out[g])  # step i - 1's outputs of group g are out
+                    for l in groups[g]:
+                        step.layer(l)
+                    ev_done[g].record(main)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(ev_done[g])
+                        for l in groups[g]:
+                            h_out[l].copy_(step.out[l], non_blocking=True)
+                        ev_out[g].record(s_out)
+                    if i + 1 < n:
+                        copy_group(i + 1, g)
+                ev_step[i % 2].record(main)
+            main.wait_stream(s_out)
+            for name, t in small[0].items():  # the step's own tensors again
+                setattr(step, name, t)
+
+        e2e_steps(args.warmup)
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_steps(args.steps)
         e1.record()
         torch.cuda.synchronize()
         barrier()
         e2e_ms = ranks_max(e0.elapsed_time(e1) / args.steps)
         e2e = {"value": kv_step * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                "ms_per_step": e2e_ms, "decode_tokens_per_s": step.B * world / (e2e_ms / 1e3),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "overlap": "copies in groups of 6 layers, pipelined across steps"}
 
     extras = {}
     if not args.no_extras:

@@ -96,6 +96,45 @@ def test_reused_plan_with_store(engine):
         assert torch.equal(out1, out2), f"layer {l} output"
 
 
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_reused_plan_in_a_captured_step(engine):
+    """A step captured as one CUDA graph (store + decode for three layers, the first planning and
+    the others reusing its plan, split contexts): replaying it equals the eager step."""
+    case, layers = _layers(5300, 3, 7, 32, 8, 128, 1, 3000)
+    bt, ctx, slots = dev_i32(case.block_tables), dev_i32(case.context_lens), dev_i32(
+        case.slot_mapping)
+    plan = pk.decode_plan(case.num_seqs, 32, layers[0]["kc0"], case.max_context_len, 256, engine)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    caches = [(d["kc0"].clone(), d["vc0"].clone()) for d in layers]
+    outs = [torch.empty_like(d["q"]) for d in layers]
+
+    def step():
+        for l, d in enumerate(layers):
+            kc, vc = caches[l]
+            pk.kv_store(d["kn"], d["vn"], slots, kc, vc)
+            pk.paged_decode(d["q"], kc, vc, bt, ctx, case.scale, out=outs[l], plan=plan,
+                            workspace=ws, reuse_plan=l > 0)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pk.get_device_error() == 0
+    for l in range(3):
+        assert torch.equal(outs[l], eager[l]), f"layer {l}"
+
+
 def test_reuse_needs_a_plan():
     with pytest.raises(ValueError):
         pk._reused(None)
