@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(kStoreThreads)
                     const int32_t* __restrict__ slot_mapping, int64_t total_vecs,
                     int32_t row_vecs, int64_t num_slots, uint4* __restrict__ k_cache,
                     uint4* __restrict__ v_cache, int* flags) {
+  // a programmatic dependent of the previous work: wait for it before any memory access
+  allow_dependent_launch();
+  grid_dependency_wait();
   const int64_t stride = (int64_t)gridDim.x * kStoreThreads;
   int64_t i = (int64_t)blockIdx.x * kStoreThreads + threadIdx.x;
   for (; i < total_vecs; i += stride * kStoreUnroll) {
@@ -77,11 +80,12 @@ cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, const int32_t*
   int64_t blocks = (total + per_block - 1) / per_block;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
-  kv_store_kernel<<<(unsigned)blocks, kStoreThreads, 0, stream>>>(
-      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slot_mapping, total,
-      row_vecs, (int64_t)cache.num_blocks * cache.block_size, reinterpret_cast<uint4*>(k_cache),
-      reinterpret_cast<uint4*>(v_cache), flags);
-  return cudaGetLastError();
+  return launch_dependent(kv_store_kernel, dim3((unsigned)blocks), dim3(kStoreThreads), 0, stream,
+                          reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
+                          slot_mapping, total, row_vecs,
+                          (int64_t)cache.num_blocks * cache.block_size,
+                          reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache),
+                          flags);
 }
 
 }  // namespace pkv

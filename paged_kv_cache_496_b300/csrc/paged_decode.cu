@@ -219,6 +219,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanParams pp) {
   // the decode grid may be scheduled now: it sets up its barriers, then waits for this grid
   allow_dependent_launch();
+  // this grid is itself a programmatic dependent of the previous work in the stream
+  grid_dependency_wait();
   if (blockIdx.x > 0) {
     store_new_rows(pp);
     return;
@@ -441,8 +443,10 @@ __global__ void __maxnreg__(168)
   }
   __syncthreads();
   // Launched as a programmatic dependent of the plan kernel: everything above overlaps the plan;
-  // nothing below reads memory before the plan (and all earlier work) has completed.
+  // nothing below reads memory before the plan (and all earlier work) has completed. The next
+  // work in the stream may then be scheduled; it waits for this grid before touching memory.
   grid_dependency_wait();
+  allow_dependent_launch();
 
   if (warp == T::kWarps) {
     // =============================== producer warp ===============================
@@ -1027,8 +1031,8 @@ cudaError_t launch_decode_plan(const DecodeArgs& a, int32_t head_groups, int32_t
     store_ctas = (int)(want < num_sms ? want : num_sms);
     if (store_ctas < 1) store_ctas = 1;
   }
-  decode_plan_kernel<<<1 + store_ctas, kPlanThreads, 0, stream>>>(pp);
-  return cudaGetLastError();
+  return launch_dependent(decode_plan_kernel, dim3(1 + store_ctas), dim3(kPlanThreads), 0, stream,
+                          pp);
 }
 
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -1097,8 +1101,8 @@ cudaError_t launch_decode_store_rows(const DecodeArgs& a, int num_sms, cudaStrea
   int64_t ctas = (chunks + 4 * kPlanThreads - 1) / (4 * kPlanThreads);
   if (ctas > num_sms) ctas = num_sms;
   if (ctas < 1) ctas = 1;
-  decode_plan_kernel<<<(unsigned)(1 + ctas), kPlanThreads, 0, stream>>>(pp);
-  return cudaGetLastError();
+  return launch_dependent(decode_plan_kernel, dim3((unsigned)(1 + ctas)), dim3(kPlanThreads), 0,
+                          stream, pp);
 }
 
 int decode_box_rows(int head_dim, int group, int block_size) {

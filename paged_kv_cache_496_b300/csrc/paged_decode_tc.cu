@@ -177,8 +177,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // Launched as a programmatic dependent of the plan grid: everything above overlaps it; nothing
-  // below reads memory before the plan (and all earlier work) has completed.
+  // below reads memory before the plan (and all earlier work) has completed. The next work in
+  // the stream may then be scheduled; it waits for this grid before touching memory.
   grid_dependency_wait();
+  allow_dependent_launch();
   const int nkv = p.num_kv_heads;
 
   if (warp == 0) {
