@@ -127,9 +127,11 @@ PKV_API int pkv_kv_store(const uint16_t* k, const uint16_t* v, const int32_t* sl
  *                          its workspace's work counters reset for such a call. With
  *                          pkv_paged_decode_store the step's store still runs, in a grid of
  *                          its own before the decode kernel. A reuse that breaks these
- *                          conditions gives wrong outputs for the sequences whose lengths
- *                          changed (never an access outside the caches or the workspace:
- *                          every table entry and context is still bounds-checked).
+ *                          conditions gives wrong outputs (never an access outside the caches
+ *                          or the workspace: every table entry and context is still
+ *                          bounds-checked, a work list longer than this call's batch allows is
+ *                          dropped and one naming a sequence outside it is skipped, both
+ *                          raising PKV_DEVERR_INTERNAL).
  */
 #define PKV_DECODE_PLAN_REUSE 1
 

@@ -38,6 +38,7 @@ DEVERR_BAD_BLOCK = 2
 DEVERR_CTX_CLAMPED = 4
 DEVERR_TIMEOUT = 8
 DEVERR_BAD_LENGTHS = 16
+DEVERR_INTERNAL = 32
 
 DECODE_ENGINE_CUDA_CORE = 1    # PKV_DECODE_ENGINE_CUDA_CORE
 DECODE_ENGINE_TENSOR_CORE = 2  # PKV_DECODE_ENGINE_TENSOR_CORE

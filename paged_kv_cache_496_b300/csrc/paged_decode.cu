@@ -454,8 +454,17 @@ __global__ void __maxnreg__(168)
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
     }
-    const uint32_t total = p.header[1] * (uint32_t)p.head_groups;
+    // The header and the work list come from this call's plan kernel or, with a reused plan,
+    // from an earlier call on the same workspace. The count is clamped to the list's capacity and
+    // items outside this call's batch are skipped (and flagged), so a reuse on the wrong
+    // workspace gives wrong outputs but never reaches memory outside the workspace or caches.
+    uint32_t n_items = p.header[1];
     const int split = (int)p.header[2];
+    if (n_items > (uint32_t)p.num_seqs * (uint32_t)p.max_splits || split < kSplitQuantum) {
+      if (lane == 0) raise_flag(p.flags, PKV_DEVERR_INTERNAL);
+      n_items = 0;
+    }
+    const uint32_t total = n_items * (uint32_t)p.head_groups;
     const int bs = p.block_size;
     // block_size is a power of two: shifts and masks instead of divisions by a runtime value
     const int lbs = __ffs(bs) - 1;
@@ -500,6 +509,11 @@ __global__ void __maxnreg__(168)
       const int x = (int)(c % (uint32_t)p.head_groups);
       const uint32_t c_next = claim();
       const int b = it.x, s = it.y;
+      if ((unsigned)b >= (unsigned)p.num_seqs || (unsigned)s >= (unsigned)p.max_splits) {
+        if (lane == 0) raise_flag(p.flags, PKV_DEVERR_INTERNAL);
+        c = c_next;
+        continue;
+      }
       int ctx = p.context_lens[b];
       ctx = ctx < p.cap_tokens ? ctx : p.cap_tokens;
       if (ctx <= 0) {

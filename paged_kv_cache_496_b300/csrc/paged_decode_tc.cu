@@ -91,6 +91,7 @@ struct TcDecodeParams {
   uint32_t* counters;  // per (sequence, kv head, output-dim quarter): chunks finished
   int* flags;
   int32_t max_blocks;
+  int32_t num_seqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
   int32_t block_size;
@@ -194,8 +195,20 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       tma_prefetch_desc(&tmap_k32);
       tma_prefetch_desc(&tmap_v32);
     }
-    const uint32_t total = p.header[1] * (uint32_t)nkv;
+    // The header and the work list come from this call's plan kernel or, with a reused plan,
+    // from an earlier call on the same workspace. The count is clamped to the list's capacity and
+    // items outside this call's batch are skipped (and flagged), so a reuse on the wrong
+    // workspace gives wrong outputs but never reaches memory outside the workspace or caches.
+    uint32_t n_items = p.header[1];
     const int split = (int)p.header[2];
+    if (n_items > (uint32_t)p.num_seqs * (uint32_t)p.max_splits || split < kSplitQuantum) {
+      if (lane == 0) raise_flag(p.flags, PKV_DEVERR_INTERNAL);
+      n_items = 0;
+    }
+    const uint32_t total = n_items * (uint32_t)nkv;
+    auto in_batch = [&](int2 r) {
+      return (unsigned)r.x < (unsigned)p.num_seqs && (unsigned)r.y < (unsigned)p.max_splits;
+    };
     const int bs = p.block_size;
     const int lbs = __ffs(bs) - 1;  // block_size is a power of two
     // Full tiles use boxes of min(block_size, 128) rows. A chunk's partial last tile of n rows
@@ -231,10 +244,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     int ctx_raw = 0, w_lo = -1, w_hi = -1;
     if (c < total) {
       it = p.items[c / (uint32_t)nkv];
-      ctx_raw = p.context_lens[it.x];
-      const int e0 = (it.y * split) >> lbs;
-      w_lo = window(it.x, e0 + lane);
-      w_hi = window(it.x, e0 + 32 + lane);
+      if (in_batch(it)) {
+        ctx_raw = p.context_lens[it.x];
+        const int e0 = (it.y * split) >> lbs;
+        w_lo = window(it.x, e0 + lane);
+        w_hi = window(it.x, e0 + 32 + lane);
+      }
     }
     uint32_t c_ahead = lane == 0 ? atomicAdd(p.header, 1u) : 0u;  // read one item later
     while (ok) {
@@ -250,7 +265,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
       const int b = it.x, s = it.y;
       const int x = (int)(c % (uint32_t)nkv);
-      const int ctx = ctx_raw < p.cap_tokens ? ctx_raw : p.cap_tokens;
+      const bool valid = in_batch(it);
+      if (!valid && lane == 0) raise_flag(p.flags, PKV_DEVERR_INTERNAL);
+      const int ctx = !valid ? -1 : ctx_raw < p.cap_tokens ? ctx_raw : p.cap_tokens;
       // the next item: its id was claimed during the previous item; its record is loaded now
       const uint32_t c_nx = __shfl_sync(kFullMask, c_ahead, 0);
       const int2 it_nx = c_nx < total ? p.items[c_nx / (uint32_t)nkv] : make_int2(0, 0);
@@ -260,14 +277,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       auto load_next = [&]() {
         if (nx_loaded) return;
         nx_loaded = true;
-        if (c_nx < total) {
+        if (c_nx < total && in_batch(it_nx)) {
           ctx_nx = p.context_lens[it_nx.x];
           const int e0 = (it_nx.y * split) >> lbs;
           w_lo_nx = window(it_nx.x, e0 + lane);
           w_hi_nx = window(it_nx.x, e0 + 32 + lane);
         }
       };
-      if (ctx <= 0) {
+      if (!valid) {
+        // outside this call's batch: nothing to read or write
+      } else if (ctx <= 0) {
         // no keys: the item's G output rows are zeros, written here without using a stage
         uint4* o = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.num_q_heads + x * G) * kDT);
         for (int i = lane; i < G * kDT / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -718,6 +737,7 @@ cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& tq,
   p.counters = a.ws.counters;
   p.flags = a.flags;
   p.max_blocks = a.max_blocks;
+  p.num_seqs = a.num_seqs;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = nkv;
   p.block_size = a.cache.block_size;

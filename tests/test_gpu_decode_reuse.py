@@ -135,6 +135,47 @@ def test_reused_plan_in_a_captured_step(engine):
         assert torch.equal(outs[l], eager[l]), f"layer {l}"
 
 
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+def test_reuse_on_a_foreign_workspace_is_bounded(engine):
+    """A reuse on a workspace that never held this call's plan stays inside its buffers: a work
+    list longer than the batch allows is dropped (0xff-filled workspace) and a list from a larger
+    batch has its extra sequences skipped, both flagged; a planning call on the same workspace
+    then gives the fresh plan's output again."""
+    case, layers = _layers(5400, 1, 9, 32, 8, 128, 1, 2000)
+    d = layers[0]
+    kc, vc = d["kc0"].clone(), d["vc0"].clone()
+    bt, ctx, slots = dev_i32(case.block_tables), dev_i32(case.context_lens), dev_i32(
+        case.slot_mapping)
+    pk.kv_store(d["kn"], d["vn"], slots, kc, vc)
+    plan = pk.decode_plan(case.num_seqs, 32, kc, case.max_context_len, 256, engine)
+    fresh = pk.paged_decode(d["q"], kc, vc, bt, ctx, case.scale, plan=plan)
+    ws = torch.full((plan.workspace_bytes,), 0xff, dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(d["q"])
+    pk.paged_decode(d["q"], kc, vc, bt, ctx, case.scale, out=out, plan=plan, workspace=ws,
+                    reuse_plan=True)
+    torch.cuda.synchronize()
+    assert pk.get_device_error() & pk.DEVERR_INTERNAL
+    assert torch.count_nonzero(out) == 0
+    again = pk.paged_decode(d["q"], kc, vc, bt, ctx, case.scale, plan=plan, workspace=ws)
+    assert pk.get_device_error() == 0
+    assert torch.equal(again, fresh)
+    # the workspace now holds the plan of the 9-sequence batch; reuse it for the first 4
+    small = pk.decode_plan(4, 32, kc, case.max_context_len, 256, engine)
+    ws2 = torch.empty(max(plan.workspace_bytes, small.workspace_bytes), dtype=torch.uint8,
+                      device="cuda")
+    pk.paged_decode(d["q"], kc, vc, bt, ctx, case.scale, plan=plan, workspace=ws2)
+    part = torch.zeros_like(d["q"][:4])
+    pk.paged_decode(d["q"][:4], kc, vc, bt[:4], ctx[:4], case.scale, out=part, plan=small,
+                    workspace=ws2, reuse_plan=True)
+    torch.cuda.synchronize()
+    assert pk.get_device_error() & pk.DEVERR_INTERNAL
+    pk.paged_decode(d["q"][:4], kc, vc, bt[:4], ctx[:4], case.scale, out=part, plan=small,
+                    workspace=ws2)
+    assert pk.get_device_error() == 0
+    assert torch.equal(part, pk.paged_decode(d["q"][:4], kc, vc, bt[:4], ctx[:4], case.scale,
+                                             plan=small))
+
+
 def test_reuse_needs_a_plan():
     with pytest.raises(ValueError):
         pk._reused(None)
