@@ -115,30 +115,11 @@ constexpr int kItemSkip = 0;  // no work (a tile past the sequence's end, or inv
 constexpr int kItemWork = 1;
 
 // Items are numbered so that the query tiles of one (sequence, kv head) are adjacent, longest
-// first: CTAs that run at the same time then share that head's K/V through L2. Invalid lengths
-// are flagged once per sequence.
+// first: CTAs that run at the same time then share that head's K/V through L2. Without a plan
+// (sparse numbering) id = (sequence x kv heads + kv head) x num_q_tiles + tile, and ids past a
+// sequence's tiles or with invalid lengths have no work; invalid lengths are flagged once per
+// sequence. The dense numbering's lookup runs inside the producer (below).
 __device__ __forceinline__ int load_item(const PrefillParams& p, int id, Item& it) {
-  if (p.item_prefix != nullptr) {
-    // dense numbering: the sequence whose range holds id (binary search over the prefix), then
-    // its kv head and query tile, the longest tile first
-    int lo = 0, hi = p.num_seqs;  // item_prefix[lo] <= id < item_prefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.item_prefix + mid) <= id) lo = mid; else hi = mid;
-    }
-    it.b = lo;
-    it.q_start = __ldg(p.cu_q + lo);
-    it.q_len = __ldg(p.cu_q + lo + 1) - it.q_start;
-    it.k_len = __ldg(p.cu_k + lo + 1) - __ldg(p.cu_k + lo);
-    const int tiles = (it.q_len + p.pos_per_tile - 1) / p.pos_per_tile;  // >= 1: listed
-    const int local = id - __ldg(p.item_prefix + lo);
-    it.g = local / tiles;
-    it.q0 = (tiles - 1 - local % tiles) * p.pos_per_tile;
-    it.P = it.k_len - it.q_len;
-    const int last_pos = min(it.q_len, it.q0 + p.pos_per_tile) - 1;
-    it.n_kt = (it.P + last_pos + 1 + kKeys - 1) / kKeys;
-    return kItemWork;
-  }
   const int qt = p.num_q_tiles - 1 - id % p.num_q_tiles;
   const int t = id / p.num_q_tiles;
   it.g = t % p.num_kv_heads;
@@ -305,14 +286,64 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       }
       return true;
     };
-    const int num_items = p.item_prefix != nullptr ? __ldg(p.item_prefix + p.num_seqs)
-                                                   : p.num_items;
+    const bool dense = p.item_prefix != nullptr;
+    const int num_items = dense ? __ldg(p.item_prefix + p.num_seqs) : p.num_items;
     int claimed = lane == 0 ? atomicAdd(p.item_counter, 1) : 0;
+    // Dense numbering: the sequence holding a claimed id is found by a 128-way search over
+    // item_prefix: each lane probes four points and ballots narrow the range 129-fold (one round
+    // of loads for up to 128 sequences, two for up to 16,641). The sequence's lengths and its
+    // first block-table window (entries 0..31, masked by the need at use) are then loaded
+    // together, so a lookup costs two or three dependent loads instead of a bisection's
+    // log2(num_seqs) + 2.
+    auto find_dense = [&](int id, Item& it, int& w) {
+      int lo = 0, hi = p.num_seqs;  // item_prefix[lo] <= id < item_prefix[hi]
+      while (hi - lo > 1) {
+        const int step = (hi - lo + 127) >> 7;
+        int v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int idx = lo + (q * 32 + lane + 1) * step;
+          v[q] = idx < hi ? __ldg(p.item_prefix + idx) : 0x7fffffff;
+        }
+        // probes are non-decreasing in (q, lane) order: the ones at or below id lead
+        int k = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) k += __popc(__ballot_sync(kFullMask, v[q] <= id));
+        hi = min(hi, lo + (k + 1) * step);
+        lo += k * step;
+      }
+      const int b = lo;
+      // lanes 0-4: cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1], item_prefix[b]
+      const int32_t* src = lane < 2 ? p.cu_q + b + lane
+                                    : (lane < 4 ? p.cu_k + b + lane - 2 : p.item_prefix + b);
+      const int f = lane < 5 ? __ldg(src) : 0;
+      w = paged && lane < p.max_blocks ? __ldg(p.block_tables + (int64_t)b * p.max_blocks + lane)
+                                       : -1;
+      it.b = b;
+      it.q_start = __shfl_sync(kFullMask, f, 0);
+      it.q_len = __shfl_sync(kFullMask, f, 1) - it.q_start;
+      it.k_len = __shfl_sync(kFullMask, f, 3) - __shfl_sync(kFullMask, f, 2);
+      const int local = id - __shfl_sync(kFullMask, f, 4);
+      const int tiles = (it.q_len + p.pos_per_tile - 1) / p.pos_per_tile;  // >= 1: listed
+      it.g = local / tiles;
+      it.q0 = (tiles - 1 - local % tiles) * p.pos_per_tile;
+      it.P = it.k_len - it.q_len;
+      const int last_pos = min(it.q_len, it.q0 + p.pos_per_tile) - 1;
+      it.n_kt = (it.P + last_pos + 1 + kKeys - 1) / kKeys;
+    };
     while (ok) {
       // next item with work, or -1; the claim after it is issued now and used later
-      int id = -1;
+      int id = -1, w0 = -1;
       Item it;
-      if (lane == 0) {
+      if (dense) {
+        id = __shfl_sync(kFullMask, claimed, 0);
+        if (id < num_items) {
+          if (lane == 0) claimed = atomicAdd(p.item_counter, 1);
+          find_dense(id, it, w0);
+        } else {
+          id = -1;
+        }
+      } else if (lane == 0) {
         while (claimed < num_items) {
           const int c = claimed;
           claimed = atomicAdd(p.item_counter, 1);
@@ -321,6 +352,8 @@ __global__ void __launch_bounds__(kThreadsP, 2)
             break;
           }
         }
+      }
+      if (lane == 0) {
         ok = mbar_wait(bar(kBarItemEmpty + (n & 1)), ((n >> 1) & 1) ^ 1);
         if (ok) {
           volatile int* sl = item_slots + (n & 1) * kItemInts;
@@ -335,16 +368,19 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
       id = __shfl_sync(kFullMask, id, 0);
       if (!ok || id < 0) break;
-      it.b = __shfl_sync(kFullMask, it.b, 0);
-      it.g = __shfl_sync(kFullMask, it.g, 0);
-      it.q_start = __shfl_sync(kFullMask, it.q_start, 0);
-      it.q_len = __shfl_sync(kFullMask, it.q_len, 0);
-      it.k_len = __shfl_sync(kFullMask, it.k_len, 0);
-      it.q0 = __shfl_sync(kFullMask, it.q0, 0);
-      it.P = __shfl_sync(kFullMask, it.P, 0);
-      it.n_kt = __shfl_sync(kFullMask, it.n_kt, 0);
+      if (!dense) {
+        it.b = __shfl_sync(kFullMask, it.b, 0);
+        it.g = __shfl_sync(kFullMask, it.g, 0);
+        it.q_start = __shfl_sync(kFullMask, it.q_start, 0);
+        it.q_len = __shfl_sync(kFullMask, it.q_len, 0);
+        it.k_len = __shfl_sync(kFullMask, it.k_len, 0);
+        it.q0 = __shfl_sync(kFullMask, it.q0, 0);
+        it.P = __shfl_sync(kFullMask, it.P, 0);
+        it.n_kt = __shfl_sync(kFullMask, it.n_kt, 0);
+      }
       int need_ent = 0;
       const int32_t* bt_row = nullptr;
+      int win_base = -1000000, win_val = -1;
       if (paged) {
         need_ent = (it.k_len + bs - 1) >> lbs;
         if (need_ent > p.max_blocks) {
@@ -352,6 +388,10 @@ __global__ void __launch_bounds__(kThreadsP, 2)
           need_ent = p.max_blocks;
         }
         bt_row = p.block_tables + (int64_t)it.b * p.max_blocks;
+        if (dense) {  // entries 0..31, loaded by the lookup
+          win_base = 0;
+          win_val = w0;
+        }
       }
       // Q half h into K-ring slot use kr + h, from that slot's lane
       const int hq = (lane + kKStages - kr % kKStages) % kKStages;
@@ -367,7 +407,6 @@ __global__ void __launch_bounds__(kThreadsP, 2)
       }
       kr += 2;
       ok = __all_sync(kFullMask, ok);
-      int win_base = -1000000, win_val = -1;
       for (int j = 0; j < it.n_kt && ok; ++j, ++t) {
         int rows[kKeys / 16];
 #pragma unroll

@@ -308,6 +308,29 @@ def test_all_decode_rows_batch(orc):
     assert_attn_close(out, ref, what="all decode rows")
 
 
+def test_dense_numbering_many_sequences(orc):
+    """400 sequences (some without new tokens): the dense lookup's search takes two rounds of
+    probes. Its output equals the sparse numbering's bit for bit and the oracle's."""
+    B = 400
+    ql = W.uniform_int(W.rng_for(75, 1), 0, 5, B).astype(np.int32)
+    prefix = W.uniform_int(W.rng_for(75, 2), 0, 200, B).astype(np.int32)
+    c = _mixed_case(75, ql, prefix, 16, 32)
+    kc, vc = dev_bf16(c["kc"]), dev_bf16(c["vc"])
+    pk.kv_store(dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["slots"]), kc, vc)
+    args = (dev_bf16(c["q"]), dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["cu_q"]),
+            dev_i32(c["cu_k"]), dev_i32(c["bt"]), c["scale"])
+    kw = dict(k_cache=kc, v_cache=vc, max_seqlen_q=int(ql.max()))
+    dense_ws = torch.empty(pk.prefill_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    sparse_ws = torch.empty(pk.PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    a = pk.paged_prefill(*args, workspace=dense_ws, **kw)
+    b = pk.paged_prefill(*args, workspace=sparse_ws, **kw)
+    assert pk.get_device_error() == 0
+    assert torch.equal(a, b)
+    ref = orc.paged_prefill(c["q"], c["k"], c["v"], c["cu_q"], c["cu_k"], c["bt"], c["kc"],
+                            c["vc"], c["scale"])
+    assert_attn_close(a, ref, what="400 sequences")
+
+
 @pytest.mark.parametrize("which", ["mixed", "no_prefix", "prefix"])
 def test_dense_and_sparse_item_numbering_agree(which):
     """With a workspace of pkv_prefill_workspace_bytes(num_seqs) the work is numbered densely
