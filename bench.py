@@ -802,8 +802,15 @@ def secondary_measurements(torch, pk, device, main_step):
         ms = timed(lambda: pk.paged_decode(layer["q"], layer["kc"], layer["vc"], layer["bt"],
                                            layer["ctx"], layer["scale"], out=layer["out"],
                                            plan=layer["plan"], workspace=layer["ws"]))
+        # the same call reusing the plan a first call made, as the layers of a step after the
+        # first do (the plan kernel then drops out of the call)
+        ms_reused = timed(lambda: pk.paged_decode(
+            layer["q"], layer["kc"], layer["vc"], layer["bt"], layer["ctx"], layer["scale"],
+            out=layer["out"], plan=layer["plan"], workspace=layer["ws"], reuse_plan=True))
         lp = profiled(*decode_profile(pk, layer["plan"].engine, "long_splitk")) or {}
         res["long_splitk_decode"] = {"ms": ms, "GB/s": layer["kv"] / ms / 1e6,
+                                     "ms_plan_reused": ms_reused,
+                                     "GB/s_plan_reused": layer["kv"] / ms_reused / 1e6,
                                      "decode_engine": decode_engine_name(pk, layer["plan"].engine),
                                      "frac_of_hbm_peak": layer["kv"] / ms / 1e6 /
                                      measured_peaks()[0],
