@@ -362,49 +362,82 @@ __device__ __forceinline__ float sum_over_tokens(float x) {
 }
 
 // The last warp to finish a (sequence, head group, output slice) of a split sequence merges all
-// chunk partials: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s, in one pass with a running
-// max and eight chunks' loads in flight. Out of line: it runs once per split sequence, and the
-// decode loop runs faster with less code in it.
+// chunk partials: o = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s, with a running max over
+// batches of chunks. A batch is one round of loads for all of the warp's outputs: lane u holds
+// chunk s0 + u's (m, l) and every lane the accumulators of its output pairs for all chunks of the
+// batch (16 loads in flight per lane); the batch maximum and the weights travel by shuffles. The
+// merge ends the launch for the sequence whose last chunk is claimed late, so its dependent L2
+// round trips (partials written by other SMs) are kept few. Out of line: it runs once per split
+// sequence, and the decode loop runs faster with less code in it.
 template <int D, int GH, int kWarps>
 __device__ __noinline__ void merge_chunks(const DecodeParams& p, int b, int x, int nsplit, int warp,
                                           int lane) {
-  for (int o = 64 * warp + 2 * lane; o < GH * D; o += kWarps * 64) {
-    const int h = o / D, d = o % D;
-    const int head = x * GH + h;
-    const int64_t base = (int64_t)b * p.max_splits * p.num_q_heads + head;
-    float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
-    for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
-      float2 ml[8], a[8];
+  constexpr int kO = (GH * D + kWarps * 64 - 1) / (kWarps * 64);  // output pairs per lane
+  constexpr int kB = 16 / kO;  // chunks per batch: 16 accumulator loads in flight per lane
+  const int o0 = 64 * warp + 2 * lane;
+  if (o0 >= GH * D) return;  // warp-uniform: GH * D is a multiple of 64
+  int64_t pbase[kO];  // partial index of chunk 0 for output k: (b, split 0, head)
+  int dd[kO];
+  float M[kO], dl[kO], n0[kO], n1[kO];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        ml[u] = make_float2(-INFINITY, 0.f);
-        a[u] = make_float2(0.f, 0.f);
-        if (sp0 + u < nsplit) {
-          const int64_t pi = base + (int64_t)(sp0 + u) * p.num_q_heads;
-          ml[u] = __ldcg(p.part_ml + pi * (D / 64) + d / 64);
-          a[u] = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pi * D + d));
-        }
+  for (int k = 0; k < kO; ++k) {
+    const int o = min(o0 + k * kWarps * 64, GH * D - 2);  // past the end: a harmless duplicate
+    dd[k] = o % D;
+    pbase[k] = (int64_t)b * p.max_splits * p.num_q_heads + x * GH + o / D;
+    M[k] = -INFINITY;
+    dl[k] = 0.f;
+    n0[k] = 0.f;
+    n1[k] = 0.f;
+  }
+  for (int s0 = 0; s0 < nsplit; s0 += kB) {
+    float2 ml[kO], a[kO][kB];
+#pragma unroll
+    for (int k = 0; k < kO; ++k) {
+      ml[k] = make_float2(-INFINITY, 0.f);
+      if (lane < kB && s0 + lane < nsplit)
+        ml[k] = __ldcg(p.part_ml + (pbase[k] + (int64_t)(s0 + lane) * p.num_q_heads) * (D / 64) +
+                       dd[k] / 64);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        a[k][u] = make_float2(0.f, 0.f);
+        if (s0 + u < nsplit)
+          a[k][u] = __ldcg(reinterpret_cast<const float2*>(
+              p.part_acc + (pbase[k] + (int64_t)(s0 + u) * p.num_q_heads) * D + dd[k]));
       }
-      float mnew = M;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mnew = fmaxf(mnew, ml[u].x);
-      if (mnew == -INFINITY) continue;
-      const float keep = M == -INFINITY ? 0.f : fast_exp2(M - mnew);
-      den *= keep;
-      n0 *= keep;
-      n1 *= keep;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wt = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mnew);
-        den += wt * ml[u].y;
-        n0 += wt * a[u].x;
-        n1 += wt * a[u].y;
-      }
-      M = mnew;
     }
+#pragma unroll
+    for (int k = 0; k < kO; ++k) {
+      float mb = ml[k].x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFullMask, mb, off));
+      const float mnew = fmaxf(M[k], mb);
+      if (mnew == -INFINITY) continue;  // nothing seen yet (warp-uniform)
+      const float keep = M[k] == -INFINITY ? 0.f : fast_exp2(M[k] - mnew);
+      const float w = ml[k].x == -INFINITY ? 0.f : fast_exp2(ml[k].x - mnew);
+      dl[k] = dl[k] * keep + w * ml[k].y;
+      float s_0 = n0[k] * keep, s_1 = n1[k] * keep;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const float wu = __shfl_sync(kFullMask, w, u);
+        s_0 += wu * a[k][u].x;
+        s_1 += wu * a[k][u].y;
+      }
+      n0[k] = s_0;
+      n1[k] = s_1;
+      M[k] = mnew;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kO; ++k) {
+    float den = dl[k];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
+    const int o = o0 + k * kWarps * 64;
+    if (o >= GH * D) continue;
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    *reinterpret_cast<__nv_bfloat162*>(p.out + ((int64_t)b * p.num_q_heads + head) * D + d) =
-        __floats2bfloat162_rn(n0 * inv, n1 * inv);
+    *reinterpret_cast<__nv_bfloat162*>(
+        p.out + ((int64_t)b * p.num_q_heads + x * GH + o / D) * D + o % D) =
+        __floats2bfloat162_rn(n0[k] * inv, n1[k] * inv);
   }
 }
 
