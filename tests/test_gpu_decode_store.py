@@ -35,6 +35,11 @@ CASES = [  # (B, Hq, Hkv, D, BS, lo, hi, zero_rows, split)
     (6, 8, 2, 64, 16, 1, 200, (0,), 0),        # D = 64
     (5, 8, 8, 128, 32, 1, 500, (), 0),         # G = 1 (one CTA per SM instance)
     (4, 8, 4, 64, 128, 5, 300, (3,), -1),      # D = 64, G = 2, auto split
+    # the tensor-core engine (D = 128, block size >= 128, G >= 4) stores inside its own grid
+    (8, 32, 8, 128, 128, 100, 900, (), 0),
+    (5, 32, 8, 128, 256, 1, 300, (0, 3), -1),  # contexts of 0 and 1
+    (4, 64, 8, 128, 128, 10, 3000, (1,), 256),  # G = 8, split: the last chunk stores
+    (6, 32, 8, 128, 128, 120, 140, (), 0),     # ctx - 1 in a context's only tile
 ]
 
 
@@ -62,10 +67,11 @@ def test_fused_store_equals_store_then_decode(orc, case):
     assert_attn_close(out, want, what=f"fused {case}")
 
 
-def test_fused_store_flags_a_slot_off_the_table():
-    c = _step_case(5, 3, 32, 8, 128, 16, 20, 40)
+@pytest.mark.parametrize("BS", [16, 128], ids=["cuda_core", "tensor_core"])
+def test_fused_store_flags_a_slot_off_the_table(BS):
+    c = _step_case(5, 3, 32, 8, 128, BS, 20, 40)
     slots = c["slots"].copy()
-    slots[1] = (slots[1] + 1) % (c["kc"].shape[0] * 16)  # not the slot of position ctx-1
+    slots[1] = (slots[1] + 1) % (c["kc"].shape[0] * BS)  # not the slot of position ctx-1
     kc, vc = dev_bf16(c["kc"]), dev_bf16(c["vc"])
     pk.get_device_error()
     pk.paged_decode_store(dev_bf16(c["q"]), dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(slots), kc,
