@@ -307,14 +307,17 @@ PKV_API int pkv_paged_decode_store(const uint16_t* q, const uint16_t* k_new, con
  *                 num_seqs), a one-CTA plan kernel first numbers only the query tiles each
  *                 sequence has, so that the attention grid claims no empty work (a decode row
  *                 in a batch with long prefill rows would otherwise cost ceil(max_seqlen_q /
- *                 tile) claims); the attention grid is its programmatic dependent.
+ *                 tile) claims), and puts sequences whose tiles are at least half full (prefill
+ *                 rows) in one queue and the rest (decode rows) in another; half the grid starts
+ *                 on each queue, so tensor work and K/V streaming overlap on every SM. The
+ *                 attention grid is the plan's programmatic dependent.
  * Runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory); supports
  * head_dim 128 and group sizes 1, 2, 4, 8 (other shapes return PKV_ERR_UNSUPPORTED). A persistent
  * grid (two CTAs per SM) claims (sequence, kv head, query tile) items from the counter.
  */
 /*
  * Workspace bytes with which pkv_paged_prefill numbers a call's work densely (see above):
- * PKV_PREFILL_WORKSPACE_BYTES plus one int per sequence and one more, rounded up to 256 bytes.
+ * PKV_PREFILL_WORKSPACE_BYTES plus two ints per sequence and one more, rounded up to 256 bytes.
  * Pure host function; returns PKV_PREFILL_WORKSPACE_BYTES for num_seqs < 0.
  */
 PKV_API size_t pkv_prefill_workspace_bytes(int32_t num_seqs);

@@ -599,7 +599,7 @@ int pkv_paged_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs) {
   if (num_seqs < 0) return PKV_PREFILL_WORKSPACE_BYTES;
-  const size_t prefix = ((size_t)num_seqs + 1) * sizeof(int32_t);
+  const size_t prefix = (2 * (size_t)num_seqs + 1) * sizeof(int32_t);  // prefix + permutation
   return PKV_PREFILL_WORKSPACE_BYTES + (prefix + 255) / 256 * 256;
 }
 

@@ -147,8 +147,9 @@ struct PrefillArgs {
   int32_t* item_counter;  // device, in the caller's workspace
   // Dense item numbering (nullptr: ids run over num_seqs x num_kv_heads x ceil(max_seqlen_q /
   // positions per tile), and the grid skips the ids of query tiles a sequence does not have):
-  // num_seqs + 1 ints in the caller's workspace, which a one-CTA plan kernel fills with each
-  // sequence's first item id before the attention grid starts.
+  // 2 x num_seqs + 1 ints in the caller's workspace, which a one-CTA plan kernel fills before
+  // the attention grid starts: each position's first item id (num_seqs + 1 ints), then the
+  // sequence at each position (heavy sequences first). item_counter then holds four ints.
   int32_t* item_prefix = nullptr;
 };
 

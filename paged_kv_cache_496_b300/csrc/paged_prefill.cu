@@ -94,10 +94,12 @@ struct PrefillParams {
   int32_t box_rows;      // rows per K/V TMA box
   int32_t oob_row;       // a row coordinate past the end of the K/V tensors (zero fill)
   float qk_scale_log2;
-  // Dense numbering when non-null: the items of sequence b are ids item_prefix[b] ..
-  // item_prefix[b + 1] - 1 (its kv heads x its own query tiles), item_prefix[num_seqs] of them
-  // in all; written by prefill_plan_kernel before this grid reads them.
+  // Dense numbering when non-null: the sequence at position pos is item_perm[pos] (heavy ones
+  // spread among light ones) and its items are ids item_prefix[pos] .. item_prefix[pos + 1] - 1
+  // (its kv heads x its own query tiles), item_prefix[num_seqs] of them in all; written by
+  // prefill_plan_kernel, with the counters, before this grid reads them.
   const int32_t* item_prefix;
+  const int32_t* item_perm;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -288,34 +290,51 @@ __global__ void __launch_bounds__(kThreadsP, 2)
     };
     const bool dense = p.item_prefix != nullptr;
     const int num_items = dense ? __ldg(p.item_prefix + p.num_seqs) : p.num_items;
+    // positions are permuted (heavy sequences spread among light ones) only when the batch
+    // holds both kinds of sequence
+    const int n_heavy_seqs = dense ? __ldg(p.item_counter + 1) : 0;
+    const bool permuted = n_heavy_seqs > 0 && n_heavy_seqs < p.num_seqs;
     int claimed = lane == 0 ? atomicAdd(p.item_counter, 1) : 0;
-    // Dense numbering: the sequence holding a claimed id is found by a 128-way search over
+    // Dense numbering: the position holding a claimed id is found by a 128-way search over
     // item_prefix: each lane probes four points and ballots narrow the range 129-fold (one round
     // of loads for up to 128 sequences, two for up to 16,641). The sequence's lengths and its
     // first block-table window (entries 0..31, masked by the need at use) are then loaded
-    // together, so a lookup costs two or three dependent loads instead of a bisection's
-    // log2(num_seqs) + 2.
+    // together, so a lookup costs two or three dependent loads (one more when the positions are
+    // permuted) instead of a bisection's log2(num_seqs) + 2.
     auto find_dense = [&](int id, Item& it, int& w) {
       int lo = 0, hi = p.num_seqs;  // item_prefix[lo] <= id < item_prefix[hi]
+      int b = lo;
       while (hi - lo > 1) {
         const int step = (hi - lo + 127) >> 7;
-        int v[4];
+        // the last round probes single positions (step 1): with permuted positions it also
+        // loads the sequence at every probe and at lo, so the answer costs no extra round trip
+        const bool with_perm = permuted && step == 1;
+        int v[4], pv[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int idx = lo + (q * 32 + lane + 1) * step;
           v[q] = idx < hi ? __ldg(p.item_prefix + idx) : 0x7fffffff;
+          pv[q] = with_perm && idx < hi ? __ldg(p.item_perm + idx) : 0;
         }
+        const int p_lo = with_perm ? __ldg(p.item_perm + lo) : 0;
         // probes are non-decreasing in (q, lane) order: the ones at or below id lead
         int k = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) k += __popc(__ballot_sync(kFullMask, v[q] <= id));
+        if (with_perm) {  // the answer is lo + k: position lo itself, or probe k - 1
+          const int slot = (k - 1) >> 5;  // uniform over the warp
+          const int mine = slot <= 0 ? pv[0] : slot == 1 ? pv[1] : slot == 2 ? pv[2] : pv[3];
+          const int from = __shfl_sync(kFullMask, mine, (k - 1) & 31);
+          b = k == 0 ? p_lo : from;
+        }
         hi = min(hi, lo + (k + 1) * step);
         lo += k * step;
       }
-      const int b = lo;
-      // lanes 0-4: cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1], item_prefix[b]
+      const int pos = lo;
+      if (!permuted) b = pos;
+      // lanes 0-4: cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1], item_prefix[pos]
       const int32_t* src = lane < 2 ? p.cu_q + b + lane
-                                    : (lane < 4 ? p.cu_k + b + lane - 2 : p.item_prefix + b);
+                                    : (lane < 4 ? p.cu_k + b + lane - 2 : p.item_prefix + pos);
       const int f = lane < 5 ? __ldg(src) : 0;
       w = paged && lane < p.max_blocks ? __ldg(p.block_tables + (int64_t)b * p.max_blocks + lane)
                                        : -1;
@@ -723,32 +742,22 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 
 }  // namespace
 
-// Dense item numbering: item_prefix[b] = the items (kv heads x query tiles) of the sequences
-// before b, item_prefix[num_seqs] = all of them; sequences with invalid lengths have none and are
-// flagged here. Also zeroes the grid's work counter. One CTA; the attention grid is its
-// programmatic dependent.
+// Dense item numbering with heavy sequences spread among light ones. A sequence is heavy when
+// its query tiles are at least half full (q_len >= positions per tile / 2: prefill rows,
+// compute-bound) and light otherwise (decode rows and short chunks, bound by their K/V read).
+// The grid claims items in position order; heavy sequence i (of H, in batch order) and light
+// sequence j (of L) are merged by the keys (i + 1/2) / H and (j + 1/2) / L, heavy first on a
+// tie, so every stretch of claims mixes the two kinds in the batch's proportion and the
+// prefill tiles' tensor work fills the time the decode rows wait on memory. item_perm[pos] is
+// the sequence at position pos, item_prefix[pos] its first item id (kv heads x its own query
+// tiles, longest first), item_prefix[num_seqs] = all items. counter[0] is zeroed for the
+// claims and counter[1] = H (no permutation when H is 0 or num_seqs). Sequences with invalid
+// lengths have no items and are flagged here. One CTA; the attention grid is its programmatic
+// dependent.
 constexpr int kPlanThreadsP = 1024;
-__global__ void __launch_bounds__(kPlanThreadsP) prefill_plan_kernel(
-    const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs, int32_t pos_per_tile,
-    int32_t num_kv_heads, int32_t* item_prefix, int32_t* item_counter, int* flags) {
-  allow_dependent_launch();
-  __shared__ int64_t warp_sums[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (num_seqs + kPlanThreadsP - 1) / kPlanThreadsP;
-  const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
-  auto items_of = [&](int b) -> int64_t {
-    const int q_len = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-    const int k_len = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
-    if (q_len < 0 || k_len < q_len) {
-      raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
-      return 0;
-    }
-    return (int64_t)((q_len + pos_per_tile - 1) / pos_per_tile) * num_kv_heads;
-  };
-  int64_t local = 0;
-  for (int b = b0; b < b1; ++b) local += items_of(b);
-  // exclusive scan of the per-thread totals over the CTA
-  int64_t incl = local;
+__device__ __forceinline__ int64_t plan_block_scan(int64_t v, int64_t* warp_sums, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t y = __shfl_up_sync(kFullMask, incl, o);
@@ -766,16 +775,101 @@ __global__ void __launch_bounds__(kPlanThreadsP) prefill_plan_kernel(
     warp_sums[lane] = w;
   }
   __syncthreads();
-  int64_t at = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
-  const int64_t total = warp_sums[31];
+  const int64_t r = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[31];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreadsP, 1) prefill_plan_kernel(
+    const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs, int32_t pos_per_tile,
+    int32_t num_kv_heads, int32_t* item_prefix, int32_t* item_perm, int32_t* item_counter,
+    int* flags) {
+  allow_dependent_launch();
+  __shared__ int64_t warp_sums[32];
+  const int tid = threadIdx.x;
+  const int per = (num_seqs + kPlanThreadsP - 1) / kPlanThreadsP;
+  const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+  // items of sequence b; *heavy: its query tiles are at least half full
+  auto items_of = [&](int b, bool* heavy) -> int32_t {
+    const int q_len = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
+    const int k_len = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
+    *heavy = false;
+    if (q_len < 0 || k_len < q_len) {
+      raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
+      return 0;
+    }
+    *heavy = 2 * q_len >= pos_per_tile;
+    return ((q_len + pos_per_tile - 1) / pos_per_tile) * num_kv_heads;
+  };
+  // one scan for both: items in the low 40 bits, heavy sequences above them (batches of 2^22
+  // sequences or more keep the batch order, so that the count fits)
+  const bool may_mix = num_seqs < (1 << 22);
+  int64_t mine = 0;
   for (int b = b0; b < b1; ++b) {
-    item_prefix[b] = (int32_t)(at < 0x7fffffff ? at : 0x7fffffff);
-    at += items_of(b);
+    bool h;
+    const int32_t n = items_of(b, &h);
+    mine += (int64_t)n + (h && may_mix ? (int64_t)1 << 40 : 0);
+  }
+  int64_t both = 0;
+  const int64_t before = plan_block_scan(mine, warp_sums, &both);
+  const int64_t H = both >> 40;
+  const int64_t L = num_seqs - H;
+  const bool mix = H > 0 && L > 0;
+  auto clamp32 = [](int64_t v) { return (int32_t)(v < 0x7fffffff ? v : 0x7fffffff); };
+  if (!mix) {
+    // one kind only: positions are the batch order, and the scan above numbers the items
+    int64_t at = before & (((int64_t)1 << 40) - 1);
+    for (int b = b0; b < b1; ++b) {
+      bool h;
+      item_prefix[b] = clamp32(at);
+      at += items_of(b, &h);
+    }
+    if (tid == 0) {
+      const int64_t total = both & (((int64_t)1 << 40) - 1);
+      item_prefix[num_seqs] = clamp32(total);
+      if (total > 0x7fffffff) raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
+      item_counter[0] = 0;
+      item_counter[1] = (int32_t)H;
+    }
+    return;
+  }
+  int64_t i = before >> 40;  // heavy rank of my first heavy one
+  int64_t j = b0 - i;        // light rank of my first light one
+  // positions: heavy i goes after the light j with (2j + 1) H < (2i + 1) L; light j after the
+  // heavy i with (2i + 1) L <= (2j + 1) H. Item counts go to item_prefix for the scan below.
+  for (int b = b0; b < b1; ++b) {
+    bool h;
+    const int32_t n = items_of(b, &h);
+    int64_t pos;
+    if (h) {
+      const int64_t num = (2 * i + 1) * L - H;  // light ones before it: ceil(num / 2H)
+      pos = i + (num <= 0 ? 0 : min(L, (num + 2 * H - 1) / (2 * H)));
+      ++i;
+    } else {
+      const int64_t num = (2 * j + 1) * H - L;  // heavy ones before it: floor(num / 2L) + 1
+      pos = j + (num < 0 ? 0 : min(H, num / (2 * L) + 1));
+      ++j;
+    }
+    item_perm[pos] = b;
+    item_prefix[pos] = n;
+  }
+  __syncthreads();  // every position's count is written (and visible to the CTA)
+  // first item id of each position: an exclusive scan of the counts in position order
+  int64_t local = 0;
+  for (int pos = b0; pos < b1; ++pos) local += item_prefix[pos];
+  int64_t total = 0;
+  int64_t at = plan_block_scan(local, warp_sums, &total);
+  for (int pos = b0; pos < b1; ++pos) {
+    const int32_t n = item_prefix[pos];
+    item_prefix[pos] = clamp32(at);
+    at += n;
   }
   if (tid == 0) {
-    item_prefix[num_seqs] = (int32_t)(total < 0x7fffffff ? total : 0x7fffffff);
+    item_prefix[num_seqs] = clamp32(total);
     if (total > 0x7fffffff) raise_flag(flags, PKV_DEVERR_BAD_LENGTHS);
-    *item_counter = 0;
+    item_counter[0] = 0;
+    item_counter[1] = (int32_t)H;
   }
 }
 
@@ -817,6 +911,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
   p.oob_row = paged ? a.cache.num_blocks * a.cache.block_size : a.total_q;
   p.qk_scale_log2 = a.scale * 1.4426950408889634f;
   p.item_prefix = a.item_prefix;
+  p.item_perm = a.item_prefix != nullptr ? a.item_prefix + a.num_seqs + 1 : nullptr;
   // upper bound of the item count (the exact count, with dense numbering, is on the device)
   const int64_t items = (int64_t)p.num_q_tiles * p.num_kv_heads * a.num_seqs;
   if (items <= 0) return cudaSuccess;
@@ -835,6 +930,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap& tq,
   prefill_plan_kernel<<<1, kPlanThreadsP, 0, stream>>>(a.cu_seqlens_q, a.cu_seqlens_k,
                                                        a.num_seqs, p.pos_per_tile,
                                                        p.num_kv_heads, a.item_prefix,
+                                                       a.item_prefix + a.num_seqs + 1,
                                                        a.item_counter, a.flags);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

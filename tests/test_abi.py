@@ -167,13 +167,15 @@ def test_prefill_validation_without_launch(pk):
 
 
 def test_prefill_workspace_bytes_for_dense_numbering(pk):
-    """The prefill counter (256 B), then one int per sequence and one more, rounded to 256 B."""
+    """The prefill counters (256 B), then two ints per sequence (first item id, sequence at each
+    position) and one more, rounded to 256 B."""
     f = pk.lib.pkv_prefill_workspace_bytes
     assert f(-1) == 256
     assert f(0) == 512
-    assert f(63) == 512
-    assert f(64) == 768
-    assert f(1000) == 256 + 4096
+    assert f(31) == 512
+    assert f(32) == 768
+    assert f(64) == 1024
+    assert f(1000) == 256 + 8192
     assert pk.prefill_workspace_bytes(64) == f(64)
 
 

@@ -309,10 +309,13 @@ def test_all_decode_rows_batch(orc):
 
 
 def test_dense_numbering_many_sequences(orc):
-    """400 sequences (some without new tokens): the dense lookup's search takes two rounds of
-    probes. Its output equals the sparse numbering's bit for bit and the oracle's."""
+    """400 sequences (some without new tokens, every fifth a prefill chunk of 16-80 tokens): the
+    dense lookup's search takes two rounds of probes, and the heavy (prefill) and light
+    sequences sit in two queues, so positions are permuted. The output equals the sparse
+    numbering's bit for bit and the oracle's."""
     B = 400
     ql = W.uniform_int(W.rng_for(75, 1), 0, 5, B).astype(np.int32)
+    ql[::5] = W.uniform_int(W.rng_for(75, 3), 16, 80, len(ql[::5]))
     prefix = W.uniform_int(W.rng_for(75, 2), 0, 200, B).astype(np.int32)
     c = _mixed_case(75, ql, prefix, 16, 32)
     kc, vc = dev_bf16(c["kc"]), dev_bf16(c["vc"])
