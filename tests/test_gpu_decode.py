@@ -328,6 +328,17 @@ def test_full_qwen3_0p6b_decode_layer(orc, engine):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
+@pytest.mark.parametrize("split", [0, 1024], ids=["auto", "split1024"])
+def test_decode_max_context(orc, engine, split):
+    """A 256K-token context beside a 64K + 17 one, short ones and a padded row: positions and
+    block ids far past 2^16, and at split 1024 one sequence's 256 chunks merged in batches.
+    Every row against the oracle."""
+    ctx = np.array([262144, 1, 700, 65553, 0, 3], np.int32)
+    _full_size(orc, ctx, 32, 8, 128, 16, 21, np.arange(len(ctx)), split=split, engine=engine)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
 def test_full_long_context_split_decode(orc, engine):
     ctx = W.decode_lengths("long_splitk_decode")
     sample = np.concatenate([[0, 3], np.arange(4, 64, 3)])
