@@ -824,31 +824,20 @@ def secondary_measurements(torch, pk, device, main_step):
         del layer
     except Exception as e:  # report, do not hide
         res["long_splitk_decode"] = {"error": repr(e)}
+    ps = None
     try:
         ps = PrefillStep(torch, pk, device)
         ps.store()
-        # Burst: timed alone after a second of idle GPU (the prefill draws enough power that the
-        # work timed just before it would otherwise set its clock), against the burst GEMM peak.
-        # Sustained: after two seconds of back-to-back calls, against the sustained GEMM peak.
-        torch.cuda.synchronize()
-        time.sleep(1.0)
+        # Burst: a few calls timed alone after the memory-bound work above, against the burst
+        # GEMM peak. The sustained figure is taken last (below): seconds at the power limit
+        # would lower the clock of whatever is timed after them. (An idle pause before the
+        # burst does not help: the clock drops to idle and the warm-up calls do not restore it.)
         ms = timed(ps.prefill)
         peak, _ = measured_tensor_peak()
         tf = ps.flops / (ms / 1e3) / 1e12
-        t_end = time.time() + 2.0
-        while time.time() < t_end:
-            for _ in range(20):
-                ps.prefill()
-            torch.cuda.synchronize()
-        ms_sus = timed(ps.prefill, reps=200)
-        peak_sus, _ = measured_tensor_peak(sustained=True)
-        tf_sus = ps.flops / (ms_sus / 1e3) / 1e12
         res["prefix_prefill"] = {"ms": ms, "TFLOP/s": tf, "frac_of_bf16_peak": tf / peak,
-                                 "timing": "burst: alone after 1 s idle",
-                                 "ms_sustained": ms_sus, "TFLOP/s_sustained": tf_sus,
-                                 "frac_of_sustained_bf16_peak": tf_sus / peak_sus,
+                                 "timing": "burst: a few calls timed alone",
                                  "new_tokens": ps.tokens, **prefill_profile_keys()}
-        del ps
     except Exception as e:
         res["prefix_prefill"] = {"error": repr(e)}
     try:
@@ -859,6 +848,22 @@ def secondary_measurements(torch, pk, device, main_step):
         res["qwen3_0p6b_step"] = _qwen3_0p6b_step(torch, pk, device)
     except Exception as e:
         res["qwen3_0p6b_step"] = {"error": repr(e)}
+    try:
+        if ps is not None and "error" not in res["prefix_prefill"]:
+            # sustained: after two seconds of back-to-back calls, against the sustained peak
+            t_end = time.time() + 2.0
+            while time.time() < t_end:
+                for _ in range(20):
+                    ps.prefill()
+                torch.cuda.synchronize()
+            ms_sus = timed(ps.prefill, reps=200)
+            peak_sus, _ = measured_tensor_peak(sustained=True)
+            tf_sus = ps.flops / (ms_sus / 1e3) / 1e12
+            res["prefix_prefill"].update({"ms_sustained": ms_sus, "TFLOP/s_sustained": tf_sus,
+                                          "frac_of_sustained_bf16_peak": tf_sus / peak_sus})
+    except Exception as e:
+        res["prefix_prefill"]["sustained_error"] = repr(e)
+    del ps
     return res
 
 
@@ -925,14 +930,12 @@ def _mixed_batch(torch, pk, device, timed):
     def call():
         pkm.paged_prefill(q, k, v, cu_q, cu_k, btd, 1 / np.sqrt(D), k_cache=kc, v_cache=vc,
                           out=out, max_seqlen_q=256)
-    torch.cuda.synchronize()
-    time.sleep(1.0)  # burst, like the prefill component: the sustained prefill runs before it
     ms = timed(call)
     qn, pre = ql.astype(np.float64), prefix.astype(np.float64)
     flops = 4.0 * D * Hq * float(np.sum(qn * pre + qn * (qn + 1) / 2))
     kv = float(kl.sum()) * Hkv * D * 4
     return {"ms": ms, "TFLOP/s": flops / ms / 1e9, "KV GB/s": kv / ms / 1e6,
-            "rows": "960 decode + 64 x 256 prefill", "timing": "burst: alone after 1 s idle"}
+            "rows": "960 decode + 64 x 256 prefill", "timing": "burst: a few calls timed alone"}
 
 
 def _decode_layer(name, torch, device):
