@@ -27,6 +27,11 @@
 //    K-major layout, and finally normalise O and store it.
 //  * The tensor core computes S for the next tile while the softmax warps work on the current
 //    one. Every wait is bounded; the CTA always frees its TMEM.
+//  * Items are claimed from a counter. With a large enough workspace a one-CTA plan kernel first
+//    numbers only the query tiles each sequence has, and orders a batch that mixes prefill rows
+//    with decode rows so that the two kinds alternate in the claims: a decode row costs this
+//    kernel a full tile's MMAs and softmax, so memory-bound and compute-bound work overlap only
+//    when they are claimed side by side.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
