@@ -334,6 +334,35 @@ def test_dense_numbering_many_sequences(orc):
     assert_attn_close(a, ref, what="400 sequences")
 
 
+def test_dense_numbering_more_sequences_than_plan_threads(orc):
+    """2,500 sequences (more than the plan CTA's 1,024 threads, so each thread places three):
+    decode rows with short contexts and every 25th a prefill chunk, merged into one claim order.
+    Equal to the sparse numbering bit for bit, and to the oracle on a sample of sequences."""
+    B = 2500
+    ql = np.ones(B, np.int32)
+    ql[::25] = W.uniform_int(W.rng_for(76, 1), 16, 48, len(ql[::25]))
+    prefix = W.uniform_int(W.rng_for(76, 2), 0, 60, B).astype(np.int32)
+    c = _mixed_case(76, ql, prefix, 16, 32)
+    kc, vc = dev_bf16(c["kc"]), dev_bf16(c["vc"])
+    pk.kv_store(dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["slots"]), kc, vc)
+    args = (dev_bf16(c["q"]), dev_bf16(c["k"]), dev_bf16(c["v"]), dev_i32(c["cu_q"]),
+            dev_i32(c["cu_k"]), dev_i32(c["bt"]), c["scale"])
+    kw = dict(k_cache=kc, v_cache=vc, max_seqlen_q=int(ql.max()))
+    dense_ws = torch.empty(pk.prefill_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    sparse_ws = torch.empty(pk.PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    a = pk.paged_prefill(*args, workspace=dense_ws, **kw)
+    b = pk.paged_prefill(*args, workspace=sparse_ws, **kw)
+    assert pk.get_device_error() == 0
+    assert torch.equal(a, b)
+    for s in (0, 1, 1023, 1024, 1025, 1250, 2047, 2048, 2475, 2499):
+        q0, q1 = int(c["cu_q"][s]), int(c["cu_q"][s + 1])
+        k0, k1 = int(c["cu_k"][s]), int(c["cu_k"][s + 1])
+        ref = orc.paged_prefill(c["q"][q0:q1], c["k"][q0:q1], c["v"][q0:q1],
+                                np.array([0, q1 - q0], np.int32), np.array([0, k1 - k0], np.int32),
+                                c["bt"][s:s + 1], c["kc"], c["vc"], c["scale"])
+        assert_attn_close(a[q0:q1], ref, what=f"sequence {s} of {B}")
+
+
 @pytest.mark.parametrize("which", ["mixed", "no_prefix", "prefix"])
 def test_dense_and_sparse_item_numbering_agree(which):
     """With a workspace of pkv_prefill_workspace_bytes(num_seqs) the work is numbered densely
